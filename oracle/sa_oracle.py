@@ -1,0 +1,143 @@
+"""ctypes front end of the C oracle (``sa_oracle.c``), fp64 results.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+Every function takes NumPy arrays: bf16 tensors as their ``uint16`` bit
+patterns, ``cu_seqlens`` / indices / tables as ``int32``, sinks as ``float32``,
+and returns ``(out, lse, key_count)`` as float64 / float64 / int32 arrays.
+``rows=(begin, end)`` restricts the work to a slice of query rows (the other
+rows of ``out`` and ``lse`` are NaN), which is how full-size workloads are
+sampled.
+"""
+from __future__ import annotations
+
+import ctypes
+import functools
+
+import numpy as np
+
+from . import build_oracle
+
+NONE, KEY0_BIAS, NULL_LOGIT = 0, 1, 2
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_F64 = ctypes.c_double
+
+
+@functools.lru_cache(maxsize=1)
+def _lib() -> ctypes.CDLL:
+    lib = ctypes.CDLL(build_oracle.build())
+    lib.oracle_window_fwd.argtypes = [
+        _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _I32, _P, _I32,
+        _F64, _P, _P, _P, _I64, _I64]
+    lib.oracle_window_fwd.restype = ctypes.c_int
+    lib.oracle_sparse_index_fwd.argtypes = [
+        _P, _P, _I64, _I32, _I32, _P, _I32, _I32, _I32, _P, _I32, _F64, _P,
+        _P, _P, _I64, _I64]
+    lib.oracle_sparse_index_fwd.restype = ctypes.c_int
+    lib.oracle_block_sparse_fwd.argtypes = [
+        _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _I32, _P, _I32,
+        _P, _I32, _F64, _P, _P, _P, _I64, _I64]
+    lib.oracle_block_sparse_fwd.restype = ctypes.c_int
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses (the ``cores`` of a CPU timing)."""
+    return int(_lib().oracle_num_threads())
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.dtype(dtype):
+        raise TypeError("expected %s, got %s" % (np.dtype(dtype), a.dtype))
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _sinks(sinks, hq):
+    if sinks is None:
+        return np.zeros(hq, np.float32)
+    return _c(sinks, np.float32)
+
+
+def window_fwd(q, k, v, cu_seqlens, window_left, window_right, sinks, mode,
+               scale, rows=None):
+    """Sliding-window attention over ``cu_seqlens``-packed sequences.
+
+    q ``[T,Hq,D]``, k/v ``[T,Hkv,D]`` (uint16 bf16 bits); returns out
+    ``[T,Hq,D]``, lse ``[Hq,T]`` and the key count per ``(token, head)``.
+    """
+    q, k, v = (_c(x, np.uint16) for x in (q, k, v))
+    cu = _c(cu_seqlens, np.int32)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    s = _sinks(sinks, hq)
+    b, e = (0, T) if rows is None else rows
+    out = np.full((T, hq, d), np.nan)
+    lse = np.full((hq, T), np.nan)
+    cnt = np.full((T, hq), -1, np.int32)
+    rc = _lib().oracle_window_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, T, hq, hkv, d,
+        int(window_left), int(window_right), _ptr(s), int(mode), float(scale),
+        _ptr(out), _ptr(lse), _ptr(cnt), b, e)
+    if rc != 0:
+        raise ValueError("oracle_window_fwd rejected its arguments")
+    return out, lse, cnt
+
+
+def sparse_index_fwd(q, kv, indices, dv, sinks, mode, scale, rows=None):
+    """Top-k index attention into one shared latent cache.
+
+    q ``[Nq,Hq,dqk]``, kv ``[nkv,dqk]`` (uint16 bf16 bits), indices
+    ``[Nq,topk]`` int32; V is the first ``dv`` columns of each kv row.
+    Returns out ``[Nq,Hq,dv]``, lse ``[Hq,Nq]``, valid-key count ``[Nq]``.
+    """
+    q, kv = _c(q, np.uint16), _c(kv, np.uint16)
+    idx = _c(indices, np.int32)
+    nq, hq, dqk = q.shape
+    topk = idx.shape[1]
+    s = _sinks(sinks, hq)
+    b, e = (0, nq) if rows is None else rows
+    out = np.full((nq, hq, dv), np.nan)
+    lse = np.full((hq, nq), np.nan)
+    cnt = np.full((nq,), -1, np.int32)
+    rc = _lib().oracle_sparse_index_fwd(
+        _ptr(q), _ptr(kv), kv.shape[0], dqk, int(dv), _ptr(idx), topk, nq, hq,
+        _ptr(s), int(mode), float(scale), _ptr(out), _ptr(lse), _ptr(cnt), b, e)
+    if rc != 0:
+        raise ValueError("oracle_sparse_index_fwd rejected its arguments")
+    return out, lse, cnt
+
+
+def block_sparse_fwd(q, k, v, batch, seq_len, block_table, block_size,
+                     cu_docs, sinks, mode, scale, rows=None):
+    """Block-sparse causal attention with a document mask.
+
+    q ``[B*S,Hq,D]``, k/v ``[B*S,Hkv,D]`` (uint16 bf16 bits), block_table
+    ``[B*S,topk]`` int32, cu_docs ``[num_docs+1]`` int32.  Returns out
+    ``[B*S,Hq,D]``, lse ``[Hq,B*S]``, key count per token ``[B*S]``.
+    """
+    q, k, v = (_c(x, np.uint16) for x in (q, k, v))
+    tab = _c(block_table, np.int32)
+    cd = _c(cu_docs, np.int32)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    s = _sinks(sinks, hq)
+    b, e = (0, T) if rows is None else rows
+    out = np.full((T, hq, d), np.nan)
+    lse = np.full((hq, T), np.nan)
+    cnt = np.full((T,), -1, np.int32)
+    rc = _lib().oracle_block_sparse_fwd(
+        _ptr(q), _ptr(k), _ptr(v), int(batch), int(seq_len), hq, hkv, d,
+        _ptr(tab), tab.shape[1], int(block_size), _ptr(cd), len(cd) - 1,
+        _ptr(s), int(mode), float(scale), _ptr(out), _ptr(lse), _ptr(cnt), b, e)
+    if rc != 0:
+        raise ValueError("oracle_block_sparse_fwd rejected its arguments")
+    return out, lse, cnt
