@@ -1,0 +1,90 @@
+"""Sink-aware varlen attention forward for GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libsa.so`` (``include/sa.h``): each
+function checks and marshals torch tensors to raw device pointers and calls the
+C entry point of the same name on the current CUDA stream.  All computation
+runs in the library's CUDA kernels; there is no CPU or PyTorch fallback, and a
+missing library raises.
+"""
+from __future__ import annotations
+
+from ._lib import SAError, lib  # noqa: F401
+from .workloads import SINK_KEY0_BIAS, SINK_NONE, SINK_NULL_LOGIT  # noqa: F401
+
+__all__ = ["sa_varlen_window_fwd", "sa_device_error", "sa_version", "SAError",
+           "SINK_NONE", "SINK_KEY0_BIAS", "SINK_NULL_LOGIT"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev_tensor(name, t, dtype, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims, got %d" % (name, ndim, t.dim()))
+    return t
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def sa_varlen_window_fwd(q, k, v, cu_seqlens, window_left, window_right, sinks,
+                         sink_mode, softmax_scale, out=None, lse=None,
+                         stream=None):
+    """Sliding-window attention with a per-head sink (C: ``sa_varlen_window_fwd``).
+
+    q ``[T,Hq,D]``, k/v ``[T,Hkv,D]`` bf16; cu_seqlens int32 ``[B+1]``; sinks
+    fp32 ``[Hq]`` (or None with ``SINK_NONE``).  Returns ``(out, lse)``:
+    bf16 ``[T,Hq,D]`` and fp32 ``[Hq,T]`` (allocated when not given).
+    """
+    torch = _torch()
+    _dev_tensor("q", q, torch.bfloat16, 3)
+    _dev_tensor("k", k, torch.bfloat16, 3)
+    _dev_tensor("v", v, torch.bfloat16, 3)
+    _dev_tensor("cu_seqlens", cu_seqlens, torch.int32, 1)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    if k.shape != (T, hkv, d) or v.shape != (T, hkv, d):
+        raise ValueError("k and v must be [T, Hkv, D] matching q")
+    if sinks is not None:
+        _dev_tensor("sinks", sinks, torch.float32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    _dev_tensor("out", out, torch.bfloat16, 3)
+    _dev_tensor("lse", lse, torch.float32, 2)
+    from ._lib import check
+    check(lib().sa_varlen_window_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_seqlens.data_ptr(),
+        cu_seqlens.numel() - 1, T, hq, hkv, d, int(window_left),
+        int(window_right), None if sinks is None else sinks.data_ptr(),
+        int(sink_mode), float(softmax_scale), out.data_ptr(), lse.data_ptr(),
+        _stream_handle(stream)))
+    return out, lse
+
+
+def sa_device_error() -> int:
+    """Synchronise the device and return (and clear) its kernel error word."""
+    import ctypes
+    from ._lib import check
+    code = ctypes.c_uint32(0)
+    check(lib().sa_device_error(ctypes.byref(code)))
+    return int(code.value)
+
+
+def sa_version() -> int:
+    return int(lib().sa_version())

@@ -1,0 +1,180 @@
+// sa_api.cu -- the C ABI declared in include/sa.h: host-side argument checks,
+// TMA descriptor encoding, the per-device error word, and dispatch to the
+// kernel launchers.  Everything here only enqueues work on the caller's stream.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "sa_internal.h"
+
+namespace sa {
+
+// Per-device word the kernels OR error codes into when a bounded wait expires.
+__device__ uint32_t g_device_error;
+
+namespace {
+thread_local char t_last_error[512] = "";
+
+bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
+                                   void*, const cuuint64_t*, const cuuint64_t*,
+                                   const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint32_t*> g_err_ptr[kMaxDevices];
+}  // namespace
+
+sa_status fail(sa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof t_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank,
+                  const void* base, const uint64_t* dims,
+                  const uint64_t* strides_bytes, const uint32_t* box,
+                  CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable (no CUDA driver?)");
+    return false;
+  }
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base),
+                  reinterpret_cast<const cuuint64_t*>(dims),
+                  reinterpret_cast<const cuuint64_t*>(strides_bytes),
+                  reinterpret_cast<const cuuint32_t*>(box), estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fail(SA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return false;
+  }
+  return true;
+}
+
+uint32_t* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return nullptr;
+  uint32_t* p = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return nullptr;
+  p = static_cast<uint32_t*>(addr);
+  g_err_ptr[dev].store(p, std::memory_order_release);
+  return p;
+}
+
+}  // namespace sa
+
+using sa::fail;
+
+extern "C" {
+
+const char* sa_last_error(void) { return sa::t_last_error; }
+
+uint32_t sa_version(void) { return (0u << 16) | 1u; }
+
+sa_status sa_device_error(uint32_t* code) {
+  if (!code) return fail(SA_ERR_INVALID_ARG, "sa_device_error: code is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess)
+    return fail(SA_ERR_CUDA, "sa_device_error: %s", cudaGetErrorString(e));
+  uint32_t v = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&v, sa::g_device_error, sizeof v);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(sa::g_device_error, &zero, sizeof zero);
+  if (e != cudaSuccess)
+    return fail(SA_ERR_CUDA, "sa_device_error: %s", cudaGetErrorString(e));
+  *code = v;
+  return SA_OK;
+}
+
+sa_status sa_varlen_window_fwd(const void* q, const void* k, const void* v,
+                               const int32_t* cu_seqlens, int32_t num_seqs,
+                               int64_t total_tokens, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               int32_t window_left, int32_t window_right,
+                               const float* sinks, int32_t sink_mode,
+                               float softmax_scale, void* out, float* lse,
+                               void* stream) {
+  const char* fn = "sa_varlen_window_fwd";
+  if (!q || !k || !v || !cu_seqlens || !out || !lse)
+    return fail(SA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (sink_mode < SA_SINK_NONE || sink_mode > SA_SINK_NULL_LOGIT)
+    return fail(SA_ERR_INVALID_ARG, "%s: unknown sink_mode %d", fn, sink_mode);
+  if (sink_mode != SA_SINK_NONE && !sinks)
+    return fail(SA_ERR_INVALID_ARG, "%s: sinks is NULL with sink_mode %d", fn, sink_mode);
+  if (num_seqs < 1)
+    return fail(SA_ERR_INVALID_ARG, "%s: num_seqs %d < 1", fn, num_seqs);
+  if (total_tokens < 0 || total_tokens > (int64_t)0x7FFFF000)
+    return fail(SA_ERR_INVALID_ARG, "%s: total_tokens %lld out of range [0, 2^31 - 4096]",
+                fn, (long long)total_tokens);
+  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0)
+    return fail(SA_ERR_INVALID_ARG,
+                "%s: num_q_heads %d must be a positive multiple of num_kv_heads %d",
+                fn, num_q_heads, num_kv_heads);
+  if (head_dim < 1)
+    return fail(SA_ERR_INVALID_ARG, "%s: head_dim %d < 1", fn, head_dim);
+  if (window_left < 0 || window_right < 0)
+    return fail(SA_ERR_INVALID_ARG, "%s: negative window (%d, %d)", fn, window_left,
+                window_right);
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale))
+    return fail(SA_ERR_INVALID_ARG, "%s: softmax_scale must be finite and > 0", fn);
+  if (!sa::aligned(q, 16) || !sa::aligned(k, 16) || !sa::aligned(v, 16) ||
+      !sa::aligned(out, 16) || !sa::aligned(lse, 4) || !sa::aligned(cu_seqlens, 4) ||
+      (sinks && !sa::aligned(sinks, 4)))
+    return fail(SA_ERR_INVALID_ARG, "%s: misaligned pointer (bf16 tensors need 16 bytes)", fn);
+  if (total_tokens == 0) return SA_OK;
+  if (!sa::device_error_word())
+    return fail(SA_ERR_CUDA, "%s: no usable CUDA device", fn);
+
+  sa::WindowArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.cu_seqlens = cu_seqlens;
+  a.num_seqs = num_seqs;
+  a.total_tokens = total_tokens;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.window_left = window_left;
+  a.window_right = window_right;
+  a.sinks = sinks;
+  a.sink_mode = sink_mode;
+  a.softmax_scale = softmax_scale;
+  a.out = out;
+  a.lse = lse;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return sa::launch_window_fwd(a);
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// sa_internal.h -- declarations shared by the C ABI (sa_api.cu) and the
+// kernel translation units.  Host-side only types; no framework types.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sa.h"
+
+namespace sa {
+
+// Records a formatted message for sa_last_error() and returns `st`.
+sa_status fail(sa_status st, const char* fmt, ...);
+
+// Encodes a tiled TMA descriptor through the driver entry point (no libcuda
+// link dependency).  Returns false with a message on failure.
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank,
+                  const void* base, const uint64_t* dims,
+                  const uint64_t* strides_bytes, const uint32_t* box,
+                  CUtensorMapSwizzle swizzle);
+
+// Address of this device's error word (a __device__ variable).
+uint32_t* device_error_word();
+
+struct WindowArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* cu_seqlens;
+  int32_t num_seqs;
+  int64_t total_tokens;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t window_left;
+  int32_t window_right;
+  const float* sinks;
+  int32_t sink_mode;
+  float softmax_scale;
+  void* out;
+  float* lse;
+  cudaStream_t stream;
+};
+
+sa_status launch_window_fwd(const WindowArgs& a);
+
+}  // namespace sa

@@ -1,0 +1,123 @@
+/*
+ * sa.h -- C ABI of the sink-aware varlen attention forward for GB300 (sm_103a).
+ *
+ * One shared library (libsa.so), plain pointers and sizes, no framework types.
+ *
+ * Operation (all entry points).  For each query row i and query head h with
+ * key set K(i) and KV head g = h / (num_q_heads / num_kv_heads):
+ *
+ *   l_j  = softmax_scale * <q[i,h,:], k[j,g,:]>                 j in K(i)
+ *   KEY0_BIAS : l_j += sinks[h] for the first key of i's sequence
+ *   LSE  = ln sum_j exp(l_j)                 (over K(i) only, natural log)
+ *   out  = sum_j exp(l_j) v[j,g,:] / den,
+ *          den = sum_j exp(l_j)               (NONE, KEY0_BIAS)
+ *          den = sum_j exp(l_j) + exp(sinks[h])   (NULL_LOGIT)
+ *   K(i) empty  ->  out = 0, LSE = -inf.
+ *
+ * Sources (page title, section):
+ *   vLLM pull 49815 "[Bugfix][MiMo] Apply vision attention sinks in the window
+ *     attention path": the sink is added to the logit of each sequence's first
+ *     key; only the first window_size + 1 queries of a sequence reach that
+ *     key; the LSE is that of the masked scaled logits, laid out
+ *     (nheads, total_q); the null logit ("s_aux") is a different operation.
+ *   afierka-intel/vllm pull 76 "Apply DeepSeek-V4 attn_sink in the XPU
+ *     sparse-MLA Triton kernel", Implementation: the null-logit sink joins the
+ *     denominator after the key loop, the LSE stays over the selected keys,
+ *     and a -inf sink is a bitwise no-op.
+ *   NeMo AutoModel "nemo_automodel.components.models.minimax_m3_vl.
+ *     cp_sparse_attn": top-k key-block selection with token-level causal and
+ *     packed-document masks (MiniMaxM3CPSparseAttention, _local_sparse_forward),
+ *     zero output for fully masked rows, 64-bit flat offsets
+ *     (_block_sel_flat_offset).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are caller-owned DEVICE memory, dense row-major (C order),
+ *     16-byte aligned.  bf16 tensors are passed as `const void*` / `void*`.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work: no host synchronisation, no device-to-host reads, no
+ *     allocation.  Results are valid once the stream reaches the call.
+ *   - sinks: fp32 [num_q_heads], finite or -inf; may be NULL when
+ *     sink_mode == SA_SINK_NONE (it is then not read).
+ *   - softmax_scale: finite and > 0.
+ *   - Arguments checkable on the host are checked before anything is
+ *     enqueued; a rejected call returns a non-OK status, enqueues nothing and
+ *     leaves a message for sa_last_error().  Errors of device-resident
+ *     content (unsorted cu_seqlens, ...) are not detected; indices and block
+ *     ids outside their range are treated as absent keys.
+ *   - Kernels never hang: each wait on the GPU is bounded; a wait that runs
+ *     out sets a bit in the device error word (sa_device_error).
+ */
+#ifndef SA_H_
+#define SA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SA_API __attribute__((visibility("default")))
+#else
+#define SA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SA_SINK_NONE = 0,       /* plain softmax over K(i)                         */
+  SA_SINK_KEY0_BIAS = 1,  /* sinks[h] added to the first key's logit         */
+  SA_SINK_NULL_LOGIT = 2  /* exp(sinks[h]) added to the denominator only     */
+} sa_sink_mode;
+
+typedef enum {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = 1, /* a null pointer, a bad size, a bad alignment     */
+  SA_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels cover    */
+  SA_ERR_CUDA = 3,        /* the CUDA runtime refused a launch / attribute   */
+  SA_ERR_WORKSPACE = 4    /* workspace missing or smaller than required      */
+} sa_status;
+
+/*
+ * Sliding-window attention over cu_seqlens-packed sequences (vLLM pull 49815,
+ * window attention path).  Key set of token i in sequence b:
+ *   { j : cu_seqlens[b] <= j < cu_seqlens[b+1],  i - window_left <= j <= i + window_right }.
+ * KEY0_BIAS biases key cu_seqlens[b] (when it lies in the window).  NULL_LOGIT
+ * and NONE are also accepted.
+ *
+ *   q          bf16 [total_tokens, num_q_heads, head_dim]
+ *   k, v       bf16 [total_tokens, num_kv_heads, head_dim]
+ *   cu_seqlens int32 [num_seqs + 1], cu_seqlens[0] = 0, non-decreasing,
+ *              cu_seqlens[num_seqs] = total_tokens (device memory)
+ *   out        bf16 [total_tokens, num_q_heads, head_dim]   (written)
+ *   lse        fp32 [num_q_heads, total_tokens]              (written)
+ * Supported: head_dim in {64, 80, 128}; num_q_heads / num_kv_heads in
+ * {1, 2, 4, 8, 16}; (128 / that ratio) + window_left + window_right <= 256;
+ * total_tokens < 2^31.  Other valid requests return SA_ERR_UNSUPPORTED.
+ */
+SA_API sa_status sa_varlen_window_fwd(const void* q, const void* k, const void* v,
+                               const int32_t* cu_seqlens, int32_t num_seqs,
+                               int64_t total_tokens, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               int32_t window_left, int32_t window_right,
+                               const float* sinks, int32_t sink_mode,
+                               float softmax_scale, void* out, float* lse,
+                               void* stream);
+
+/* Message of the last non-OK status returned on this host thread ("" if none). */
+SA_API const char* sa_last_error(void);
+
+/*
+ * Device error word of the current device: bits set by kernels whose bounded
+ * waits ran out (1 load, 2 MMA, 4 buffer release, 8 drain, 16 config).
+ * Synchronises the device, reads the word into *code and clears it.
+ */
+SA_API sa_status sa_device_error(uint32_t* code);
+
+/* Library version as (major << 16) | minor. */
+SA_API uint32_t sa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA_H_ */

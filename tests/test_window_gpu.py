@@ -1,0 +1,136 @@
+"""Parity of the sliding-window CUDA path (through the C ABI) with the oracle.
+
+Covers the tiny two-sequence case in every sink mode, ragged sizes that span
+several tiles with a ragged tail, every supported GQA ratio and head dim,
+asymmetric and zero windows, length-1 sequences (with a -inf KEY0 sink: an
+empty key set), the bitwise no-op cases, and the full-size vision-tower and
+GQA workloads in the launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+
+from attention_head_sinks_gb300 import workloads as W
+from oracle import sa_oracle as O
+from tests.gpu_util import LSE_TOL, REL_L2_TOL, compare, dev
+
+pytestmark = pytest.mark.gpu
+
+NONE, KEY0, NULL = W.SINK_NONE, W.SINK_KEY0_BIAS, W.SINK_NULL_LOGIT
+
+
+def gpu_run(c, mode, sinks=None, stream=None):
+    import torch
+    import attention_head_sinks_gb300 as sa
+    s = c.sinks if sinks is None else sinks
+    out, lse = sa.sa_varlen_window_fwd(
+        dev(c.q), dev(c.k), dev(c.v), dev(c.cu_seqlens), c.window_left,
+        c.window_right, dev(s), mode, c.scale, stream=stream)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def oracle_run(c, mode, sinks=None):
+    o, l, _ = O.window_fwd(c.q, c.k, c.v, c.cu_seqlens, c.window_left,
+                           c.window_right, c.sinks if sinks is None else sinks,
+                           mode, c.scale)
+    return o, l
+
+
+def check(c, mode, sinks=None):
+    out, lse = gpu_run(c, mode, sinks)
+    ro, rl = oracle_run(c, mode, sinks)
+    rel, dl = compare(out, lse, ro, rl)
+    assert rel <= REL_L2_TOL and dl <= LSE_TOL, (c.name, mode, rel, dl)
+    return out, lse
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    import attention_head_sinks_gb300 as sa
+    yield
+    assert sa.sa_device_error() == 0
+
+
+@pytest.mark.parametrize("mode", [NONE, KEY0, NULL])
+def test_tiny_two_sequences(mode):
+    check(W.tiny_window(mode), mode)
+
+
+@pytest.mark.parametrize("mode", [KEY0, NULL])
+def test_tiny_neg_inf_sinks(mode):
+    c = W.tiny_window(mode)
+    check(c, mode, sinks=np.full(c.num_q_heads, -np.inf, np.float32))
+
+
+def test_neg_inf_null_logit_is_bitwise_no_sink():
+    import torch
+    c = W.gqa_window(seed=77)
+    ninf = np.full(c.num_q_heads, -np.inf, np.float32)
+    o0, l0 = gpu_run(c, NONE)
+    o2, l2 = gpu_run(c, NULL, sinks=ninf)
+    assert torch.equal(o0.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l0, l2)
+
+
+def test_zero_key0_sink_is_bitwise_no_sink():
+    import torch
+    c = W.tiny_window(seed=78)
+    zero = np.zeros(c.num_q_heads, np.float32)
+    o0, l0 = gpu_run(c, NONE)
+    o1, l1 = gpu_run(c, KEY0, sinks=zero)
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16))
+    assert torch.equal(l0, l1)
+
+
+RAGGED = [
+    # lengths, hq, hkv, d, wl, wr
+    ([300, 1, 77, 129, 1000, 5], 4, 4, 80, 64, 64),
+    ([1, 1, 2, 63, 64, 65, 500], 8, 2, 80, 64, 64),
+    ([700, 333], 16, 4, 80, 64, 64),
+    ([513, 17, 1030], 8, 1, 64, 64, 64),
+    ([257, 31, 400], 16, 1, 128, 60, 60),
+    ([200, 201], 4, 2, 128, 64, 64),
+    ([129, 255, 3], 2, 2, 64, 100, 28),
+    ([90, 45], 2, 1, 80, 3, 5),
+    ([64, 10], 4, 4, 80, 0, 0),
+]
+
+
+@pytest.mark.parametrize("mode", [NONE, KEY0, NULL])
+@pytest.mark.parametrize("ci", range(len(RAGGED)))
+def test_ragged_shapes(ci, mode):
+    lengths, hq, hkv, d, wl, wr = RAGGED[ci]
+    c = W.window_case(lengths, hq, hkv, d, wl, (-1.0, 3.0), mode, 2000 + ci,
+                      "ragged%d" % ci, window_right=wr)
+    check(c, mode)
+
+
+def test_length_one_sequence_with_neg_inf_key0_is_empty():
+    c = W.window_case([1, 40, 1, 90], 4, 2, 80, 64, (-1, 1), KEY0, 2100, "len1")
+    ninf = np.full(c.num_q_heads, -np.inf, np.float32)
+    out, lse = check(c, KEY0, sinks=ninf)
+    assert (out[0] == 0).all() and (out[41] == 0).all()
+    assert bool(lse[:, 0].isneginf().all()) and bool(lse[:, 41].isneginf().all())
+
+
+def test_repeatable_and_stream_aware():
+    import torch
+    c = W.window_case([500, 300], 16, 4, 80, 64, (-1, 3), KEY0, 2200, "rep")
+    s = torch.cuda.Stream()
+    o1, l1 = gpu_run(c, KEY0, stream=s)
+    o2, l2 = gpu_run(c, KEY0)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("tokens", [4096, 16384])
+@pytest.mark.parametrize("mode", [KEY0, NONE])
+def test_vision_tower_window_block(tokens, mode):
+    check(W.vision_window(tokens, mode), mode)
+
+
+@pytest.mark.parametrize("mode", [KEY0, NONE])
+def test_gqa_window_16k(mode):
+    c = W.gqa_window(mode)
+    assert min(np.diff(c.cu_seqlens)) < c.window_left
+    check(c, mode)
