@@ -11,7 +11,8 @@ from __future__ import annotations
 from ._lib import SAError, lib  # noqa: F401
 from .workloads import SINK_KEY0_BIAS, SINK_NONE, SINK_NULL_LOGIT  # noqa: F401
 
-__all__ = ["sa_varlen_window_fwd", "sa_device_error", "sa_version", "SAError",
+__all__ = ["sa_varlen_window_fwd", "sa_sparse_index_fwd",
+           "sa_sparse_index_workspace_size", "sa_device_error", "sa_version", "SAError",
            "SINK_NONE", "SINK_KEY0_BIAS", "SINK_NULL_LOGIT"]
 
 
@@ -73,6 +74,58 @@ def sa_varlen_window_fwd(q, k, v, cu_seqlens, window_left, window_right, sinks,
         cu_seqlens.numel() - 1, T, hq, hkv, d, int(window_left),
         int(window_right), None if sinks is None else sinks.data_ptr(),
         int(sink_mode), float(softmax_scale), out.data_ptr(), lse.data_ptr(),
+        _stream_handle(stream)))
+    return out, lse
+
+
+def sa_sparse_index_workspace_size(num_queries, num_q_heads, dv, topk) -> int:
+    """Workspace bytes ``sa_sparse_index_fwd`` needs (C: same name)."""
+    return int(lib().sa_sparse_index_workspace_size(
+        int(num_queries), int(num_q_heads), int(dv), int(topk)))
+
+
+def sa_sparse_index_fwd(q, kv_latent, indices, dv, sinks, sink_mode,
+                        softmax_scale, out=None, lse=None, workspace=None,
+                        stream=None):
+    """Top-k index attention into one shared latent cache (C:
+    ``sa_sparse_index_fwd``).
+
+    q ``[Nq,Hq,dqk]`` and kv_latent ``[nkv,dqk]`` bf16, indices int32
+    ``[Nq,topk]`` (-1 padded), sinks fp32 ``[Hq]`` (or None with
+    ``SINK_NONE``).  V is the first ``dv`` latent columns.  Returns
+    ``(out, lse)``: bf16 ``[Nq,Hq,dv]`` and fp32 ``[Hq,Nq]``.  ``workspace``
+    (a CUDA uint8 tensor) is allocated by torch when not given.
+    """
+    torch = _torch()
+    _dev_tensor("q", q, torch.bfloat16, 3)
+    _dev_tensor("kv_latent", kv_latent, torch.bfloat16, 2)
+    _dev_tensor("indices", indices, torch.int32, 2)
+    nq, hq, dqk = q.shape
+    nkv = kv_latent.shape[0]
+    topk = indices.shape[1]
+    if kv_latent.shape[1] != dqk or indices.shape[0] != nq:
+        raise ValueError("kv_latent must be [nkv, dqk] and indices [Nq, topk]")
+    if sinks is not None:
+        _dev_tensor("sinks", sinks, torch.float32, 1)
+    if out is None:
+        out = torch.empty((nq, hq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((hq, nq), dtype=torch.float32, device=q.device)
+    need = sa_sparse_index_workspace_size(nq, hq, dv, topk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _dev_tensor("out", out, torch.bfloat16, 3)
+    _dev_tensor("lse", lse, torch.float32, 2)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _dev_tensor("workspace", workspace, torch.uint8, 1)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    from ._lib import check
+    check(lib().sa_sparse_index_fwd(
+        q.data_ptr(), kv_latent.data_ptr(), nkv, dqk, int(dv),
+        indices.data_ptr(), topk, nq, hq,
+        None if sinks is None else sinks.data_ptr(), int(sink_mode),
+        float(softmax_scale), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes,
         _stream_handle(stream)))
     return out, lse
 

@@ -177,4 +177,71 @@ sa_status sa_varlen_window_fwd(const void* q, const void* k, const void* v,
   return sa::launch_window_fwd(a);
 }
 
+size_t sa_sparse_index_workspace_size(int32_t num_queries, int32_t num_q_heads,
+                                      int32_t dv, int32_t topk) {
+  if (num_queries <= 0 || num_q_heads <= 0 || dv != 512 || topk <= 0) return 0;
+  return sa::sparse_index_workspace_bytes(num_queries, num_q_heads, topk);
+}
+
+sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent, int64_t num_kv,
+                              int32_t dqk, int32_t dv, const int32_t* indices,
+                              int32_t topk, int32_t num_queries, int32_t num_q_heads,
+                              const float* sinks, int32_t sink_mode, float softmax_scale,
+                              void* out, float* lse, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  const char* fn = "sa_sparse_index_fwd";
+  if (!q || !kv_latent || !indices || !out || !lse)
+    return fail(SA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (sink_mode < SA_SINK_NONE || sink_mode > SA_SINK_NULL_LOGIT)
+    return fail(SA_ERR_INVALID_ARG, "%s: unknown sink_mode %d", fn, sink_mode);
+  if (sink_mode != SA_SINK_NONE && !sinks)
+    return fail(SA_ERR_INVALID_ARG, "%s: sinks is NULL with sink_mode %d", fn, sink_mode);
+  if (num_queries < 0 || num_q_heads < 1 || topk < 0 || num_kv < 1 || dqk < 1 || dv < 1 ||
+      dv > dqk)
+    return fail(SA_ERR_INVALID_ARG,
+                "%s: bad sizes (num_queries %d, num_q_heads %d, topk %d, num_kv %lld, dqk %d, dv %d)",
+                fn, num_queries, num_q_heads, topk, (long long)num_kv, dqk, dv);
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale))
+    return fail(SA_ERR_INVALID_ARG, "%s: softmax_scale must be finite and > 0", fn);
+  if (!sa::aligned(q, 16) || !sa::aligned(kv_latent, 16) || !sa::aligned(out, 16) ||
+      !sa::aligned(lse, 4) || !sa::aligned(indices, 4) || (sinks && !sa::aligned(sinks, 4)) ||
+      (workspace && !sa::aligned(workspace, 16)))
+    return fail(SA_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  if (sink_mode == SA_SINK_KEY0_BIAS)
+    return fail(SA_ERR_UNSUPPORTED, "%s: KEY0_BIAS needs a sequence start; an index list has none",
+                fn);
+  if (num_kv >= ((int64_t)1 << 31))
+    return fail(SA_ERR_UNSUPPORTED, "%s: num_kv %lld >= 2^31", fn, (long long)num_kv);
+  if (topk > sa::sparse_index_max_topk())
+    return fail(SA_ERR_UNSUPPORTED, "%s: topk %d > %d", fn, topk, sa::sparse_index_max_topk());
+  if (num_queries > 0 && dqk == 576 && dv == 512) {
+    const size_t need = sa::sparse_index_workspace_bytes(num_queries, num_q_heads, topk);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+      return fail(SA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                  workspace ? workspace_bytes : (size_t)0);
+  }
+  if (num_queries == 0) return SA_OK;
+  if (!sa::device_error_word())
+    return fail(SA_ERR_CUDA, "%s: no usable CUDA device", fn);
+  sa::IndexArgs a;
+  a.q = q;
+  a.kv = kv_latent;
+  a.num_kv = num_kv;
+  a.dqk = dqk;
+  a.dv = dv;
+  a.indices = indices;
+  a.topk = topk;
+  a.num_queries = num_queries;
+  a.num_q_heads = num_q_heads;
+  a.sinks = sinks;
+  a.sink_mode = sink_mode;
+  a.softmax_scale = softmax_scale;
+  a.out = out;
+  a.lse = lse;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return sa::launch_sparse_index_fwd(a);
+}
+
 }  // extern "C"

@@ -45,4 +45,28 @@ struct WindowArgs {
 
 sa_status launch_window_fwd(const WindowArgs& a);
 
+struct IndexArgs {
+  const void* q;
+  const void* kv;
+  int64_t num_kv;
+  int32_t dqk;
+  int32_t dv;
+  const int32_t* indices;
+  int32_t topk;
+  int32_t num_queries;
+  int32_t num_q_heads;
+  const float* sinks;
+  int32_t sink_mode;
+  float softmax_scale;
+  void* out;
+  float* lse;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+};
+
+size_t sparse_index_workspace_bytes(int32_t num_queries, int32_t num_q_heads, int32_t topk);
+int sparse_index_max_topk();
+sa_status launch_sparse_index_fwd(const IndexArgs& a);
+
 }  // namespace sa

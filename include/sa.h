@@ -103,6 +103,41 @@ SA_API sa_status sa_varlen_window_fwd(const void* q, const void* k, const void* 
                                float softmax_scale, void* out, float* lse,
                                void* stream);
 
+/*
+ * Top-k index attention into one shared latent KV cache (MLA decode) -- the
+ * sparse-MLA kernel of afierka-intel/vllm pull 76 "Apply DeepSeek-V4 attn_sink
+ * in the XPU sparse-MLA Triton kernel".  Query q attends exactly the keys
+ * listed in indices[q, :]; entries outside [0, num_kv) (the -1 padding, at any
+ * position) are absent; a repeated index counts twice.  K is the whole latent
+ * row, V its first dv columns, shared by all query heads.  NONE and NULL_LOGIT
+ * (LSE over the listed keys only) are supported; KEY0_BIAS has no first key
+ * here and returns SA_ERR_UNSUPPORTED.
+ *
+ *   q          bf16 [num_queries, num_q_heads, dqk]
+ *   kv_latent  bf16 [num_kv, dqk]
+ *   indices    int32 [num_queries, topk]
+ *   out        bf16 [num_queries, num_q_heads, dv]            (written)
+ *   lse        fp32 [num_q_heads, num_queries]                 (written)
+ *   workspace  device scratch of at least
+ *              sa_sparse_index_workspace_size(num_queries, num_q_heads, dv, topk)
+ *              bytes (may be NULL when that size is 0), 16-byte aligned; its
+ *              contents need no initialisation and are overwritten.
+ * Supported: dqk = 576, dv = 512, topk <= 8192, num_kv < 2^31.
+ */
+SA_API sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent,
+                                     int64_t num_kv, int32_t dqk, int32_t dv,
+                                     const int32_t* indices, int32_t topk,
+                                     int32_t num_queries, int32_t num_q_heads,
+                                     const float* sinks, int32_t sink_mode,
+                                     float softmax_scale, void* out, float* lse,
+                                     void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/* Workspace bytes sa_sparse_index_fwd needs for these sizes (0 if none). */
+SA_API size_t sa_sparse_index_workspace_size(int32_t num_queries,
+                                             int32_t num_q_heads, int32_t dv,
+                                             int32_t topk);
+
 /* Message of the last non-OK status returned on this host thread ("" if none). */
 SA_API const char* sa_last_error(void);
 

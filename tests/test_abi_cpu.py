@@ -84,3 +84,44 @@ def test_python_binding_rejects_cpu_tensors():
     cu = torch.tensor([0, 4], dtype=torch.int32)
     with pytest.raises(ValueError):
         sa.sa_varlen_window_fwd(q, q, q, cu, 8, 8, None, 0, 0.1)
+
+
+def _index_call(lib, **kw):
+    a = dict(q=16, kv=16, nkv=1000, dqk=576, dv=512, idx=16, topk=2048, nq=64,
+             hq=128, sinks=16, mode=2, scale=0.04, out=16, lse=16, ws=16,
+             ws_bytes=1 << 40)
+    a.update(kw)
+    return lib.sa_sparse_index_fwd(
+        a["q"], a["kv"], a["nkv"], a["dqk"], a["dv"], a["idx"], a["topk"], a["nq"],
+        a["hq"], a["sinks"], a["mode"], a["scale"], a["out"], a["lse"], a["ws"],
+        a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(q=None), 1, "NULL"),
+    (dict(mode=5), 1, "sink_mode"),
+    (dict(sinks=None), 1, "sinks is NULL"),
+    (dict(nkv=0), 1, "bad sizes"),
+    (dict(dv=600), 1, "bad sizes"),
+    (dict(kv=24), 1, "misaligned"),
+    (dict(mode=1), 2, "KEY0_BIAS"),
+    (dict(nkv=1 << 31), 2, "num_kv"),
+    (dict(topk=9000), 2, "topk"),
+    (dict(ws=None), 4, "workspace"),
+    (dict(ws_bytes=1000), 4, "workspace"),
+])
+def test_sparse_index_rejects_bad_arguments(lib, kw, status, needle):
+    assert _index_call(lib, **kw) == status
+    assert needle in lib.sa_last_error().decode()
+
+
+def test_sparse_index_workspace_size(lib):
+    # 8 slices of 256 slots: (O partial 512 + m, l) fp32 per (query, slice, head)
+    assert lib.sa_sparse_index_workspace_size(64, 128, 512, 2048) == \
+        64 * 8 * 128 * 514 * 4
+    assert lib.sa_sparse_index_workspace_size(64, 128, 512, 256) == 0
+    assert lib.sa_sparse_index_workspace_size(0, 128, 512, 2048) == 0
+
+
+def test_sparse_index_empty_batch_is_a_no_op(lib):
+    assert _index_call(lib, nq=0) == 0

@@ -1,0 +1,125 @@
+"""Parity of the sparse-index (MLA decode) CUDA path with the oracle.
+
+Covers the full 64-query x 128-head decode workload with 1/4/16/128/512/2048
+valid keys per query (afierka-intel/vllm pull 76, Why / Test plan), the
+-inf no-op, empty rows, -1 padding anywhere in the row, out-of-range and
+repeated indices, lists that end inside a slice, head counts below and above
+one 128-row block, and workspace reuse across calls.
+"""
+import numpy as np
+import pytest
+
+from attention_head_sinks_gb300 import workloads as W
+from oracle import sa_oracle as O
+from tests.gpu_util import LSE_TOL, REL_L2_TOL, compare, dev
+
+pytestmark = pytest.mark.gpu
+
+NONE, NULL = W.SINK_NONE, W.SINK_NULL_LOGIT
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    import attention_head_sinks_gb300 as sa
+    yield
+    assert sa.sa_device_error() == 0
+
+
+def gpu_run(c, mode, sinks=None, indices=None, workspace=None):
+    import torch
+    import attention_head_sinks_gb300 as sa
+    s = c.sinks if sinks is None else sinks
+    idx = c.indices if indices is None else indices
+    out, lse = sa.sa_sparse_index_fwd(dev(c.q), dev(c.kv), dev(idx), c.dv, dev(s),
+                                      mode, c.scale, workspace=workspace)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def check(c, mode, sinks=None, indices=None, workspace=None):
+    out, lse = gpu_run(c, mode, sinks, indices, workspace)
+    ro, rl, _ = O.sparse_index_fwd(c.q, c.kv, c.indices if indices is None else indices,
+                                   c.dv, c.sinks if sinks is None else sinks, mode,
+                                   c.scale)
+    rel, dl = compare(out, lse, ro, rl)
+    assert rel <= REL_L2_TOL and dl <= LSE_TOL, (c.name, mode, rel, dl)
+    return out, lse
+
+
+@pytest.mark.parametrize("mode", [NULL, NONE])
+def test_mla_sparse_decode_full(mode):
+    check(W.mla_sparse_decode(mode), mode)
+
+
+def test_mla_sparse_decode_per_valid_count():
+    """Each valid-key class separately meets the bar (rows of one class)."""
+    c = W.mla_sparse_decode(NULL, seed=1104)
+    out, lse = gpu_run(c, NULL)
+    ro, rl, n = O.sparse_index_fwd(c.q, c.kv, c.indices, c.dv, c.sinks, NULL, c.scale)
+    for cnt in W.MLA_VALID_COUNTS:
+        rows = np.nonzero(n == cnt)[0]
+        rel, dl = compare(out, lse, ro, rl, rows=rows)
+        assert rel <= REL_L2_TOL and dl <= LSE_TOL, (cnt, rel, dl)
+
+
+def test_neg_inf_sink_is_bitwise_no_sink():
+    import torch
+    c = W.mla_sparse_decode(NULL, seed=1204)
+    ninf = np.full(c.num_q_heads, -np.inf, np.float32)
+    o0, l0 = gpu_run(c, NONE)
+    o2, l2 = gpu_run(c, NULL, sinks=ninf)
+    assert torch.equal(o0.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l0, l2)
+
+
+def ragged_indices(rng, nq, nkv, topk, counts):
+    idx = np.full((nq, topk), -1, np.int32)
+    for q in range(nq):
+        c = counts[q % len(counts)]
+        sel = rng.choice(nkv, size=c, replace=False).astype(np.int32)
+        pos = np.sort(rng.choice(topk, size=c, replace=False))
+        idx[q, pos] = sel                      # -1 padding anywhere in the row
+    return idx
+
+
+@pytest.mark.parametrize("hq", [128, 64, 192])
+@pytest.mark.parametrize("mode", [NULL, NONE])
+def test_ragged_lists(hq, mode):
+    rng = np.random.default_rng(hq)
+    counts = [0, 1, 3, 17, 255, 256, 257, 511, 600, 1000]
+    c = W.index_case(10, hq, 576, 512, 5000, 1024, counts, (-2.2, 2.49), mode,
+                     3000 + hq, "ragged_idx")
+    idx = ragged_indices(rng, 10, 5000, 1024, counts)
+    idx[3, 7] = 5000          # out of range: absent
+    idx[4, 9] = -123          # negative: absent
+    out, lse = check(c, mode, indices=idx)
+    assert (out[0] == 0).all() and bool(lse[:, 0].isneginf().all())
+
+
+def test_repeated_index_counts_twice():
+    c = W.index_case(4, 128, 576, 512, 700, 300, (5, 40, 260, 299), (-2.2, 2.49),
+                     NULL, 3100, "dup")
+    idx = c.indices.copy()
+    idx[1, 40] = idx[1, 0]
+    idx[2, 270] = idx[2, 3]
+    check(c, NULL, indices=idx)
+
+
+@pytest.mark.parametrize("topk", [1, 16, 200, 256, 257, 513])
+def test_list_lengths(topk):
+    c = W.index_case(6, 128, 576, 512, 3000, topk, (topk, 1, topk // 2 + 1),
+                     (-2.2, 2.49), NULL, 3200 + topk, "len")
+    check(c, NULL)
+
+
+def test_workspace_reuse_with_stale_contents():
+    import torch
+    import attention_head_sinks_gb300 as sa
+    c = W.index_case(8, 128, 576, 512, 4000, 1024, (1000, 3, 700, 0), (-2.2, 2.49),
+                     NULL, 3300, "reuse")
+    ws = torch.empty(sa.sa_sparse_index_workspace_size(8, 128, 512, 1024),
+                     dtype=torch.uint8, device="cuda")
+    check(c, NULL, workspace=ws)
+    # second call: the multi-slice rows become single-slice and vice versa
+    idx2 = c.indices[::-1].copy()
+    check(c, NULL, indices=idx2, workspace=ws)
