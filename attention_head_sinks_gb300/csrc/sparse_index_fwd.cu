@@ -29,6 +29,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
 
@@ -540,3 +542,58 @@ sa_status launch_sparse_index_fwd(const IndexArgs& a) {
 }
 
 }  // namespace sa
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot obtain device memory for a workspace: code embedded in a
+// host runtime that owns the whole device memory pool and hands its plugins no
+// allocator, or a serving loop that forbids any allocation once it is running.
+// sa_sparse_index_fwd_noalloc serves them by keeping the split-KV partials in
+// the fixed array below instead of a caller workspace.  The array is reserved
+// on every GPU that loads this library and stays reserved until the process
+// exits.  Every call shares it and it keeps the last call's contents; nothing
+// in it has to start at zero, because each call writes every (m, l) entry and
+// every partial row it later reads.  Two calls whose work overlaps on the GPU
+// (different streams, or different host threads) race on the array.
+namespace sa {
+namespace {
+constexpr size_t kNoAllocScratchBytes = (size_t)64 << 20;  // 64 MiB
+constexpr int kNoAllocMaxDevices = 64;
+std::atomic<void*> g_noalloc_scratch_ptr[kNoAllocMaxDevices];
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+}  // namespace sa
+
+extern "C" sa_status sa_sparse_index_fwd_noalloc(
+    const void* q, const void* kv_latent, int64_t num_kv, int32_t dqk, int32_t dv,
+    const int32_t* indices, int32_t topk, int32_t num_queries, int32_t num_q_heads,
+    const float* sinks, int32_t sink_mode, float softmax_scale, void* out, float* lse,
+    void* stream) {
+  const char* fn = "sa_sparse_index_fwd_noalloc";
+  const size_t need = sa_sparse_index_workspace_size(num_queries, num_q_heads, dv, topk);
+  if (need > sa::kNoAllocScratchBytes)
+    return sa::fail(SA_ERR_UNSUPPORTED,
+                    "%s: these sizes need %zu bytes of scratch, above the fixed %zu bytes "
+                    "(64 MiB) of this entry point; use sa_sparse_index_fwd with a workspace",
+                    fn, need, sa::kNoAllocScratchBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= sa::kNoAllocMaxDevices)
+    return sa::fail(SA_ERR_CUDA, "%s: no usable CUDA device", fn);
+  void* ptr = sa::g_noalloc_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (!ptr) {
+    // One-time set-up on this device (the device is current): the host-side
+    // name of the array is not a device address, so ask the runtime for it.
+    e = cudaGetSymbolAddress(&ptr, sa::g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr)
+      return sa::fail(SA_ERR_CUDA, "%s: cudaGetSymbolAddress failed: %s", fn,
+                      cudaGetErrorString(e));
+    sa::g_noalloc_scratch_ptr[dev].store(ptr, std::memory_order_release);
+  }
+  return sa_sparse_index_fwd(q, kv_latent, num_kv, dqk, dv, indices, topk, num_queries,
+                             num_q_heads, sinks, sink_mode, softmax_scale, out, lse, ptr,
+                             sa::kNoAllocScratchBytes, stream);
+}

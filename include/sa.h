@@ -138,6 +138,31 @@ SA_API size_t sa_sparse_index_workspace_size(int32_t num_queries,
                                              int32_t num_q_heads, int32_t dv,
                                              int32_t topk);
 
+/*
+ * Allocation-free variant of sa_sparse_index_fwd.  The pages have no
+ * counterpart: it exists for callers that cannot allocate device memory for a
+ * workspace -- for example code running inside a host runtime that owns the
+ * whole device memory pool and gives its plugins no allocator, or a serving
+ * loop that must not allocate once it runs.  Arguments, layouts, results and
+ * errors are those of sa_sparse_index_fwd, without the workspace.
+ *
+ * The split-KV scratch is a fixed 64 MiB array inside the library, reserved on
+ * every GPU that loads the library until the process exits.  Sizes whose
+ * sa_sparse_index_workspace_size() exceeds 64 MiB are rejected with
+ * SA_ERR_UNSUPPORTED and a message; use sa_sparse_index_fwd for them.  The
+ * call itself allocates nothing.  The first call on each device looks up the
+ * array's device address once (make that first call before any stream
+ * capture).  All calls share the array: calls whose work overlaps on the GPU
+ * (other streams or host threads) race and must be serialised by the caller.
+ */
+SA_API sa_status sa_sparse_index_fwd_noalloc(const void* q, const void* kv_latent,
+                                             int64_t num_kv, int32_t dqk, int32_t dv,
+                                             const int32_t* indices, int32_t topk,
+                                             int32_t num_queries, int32_t num_q_heads,
+                                             const float* sinks, int32_t sink_mode,
+                                             float softmax_scale, void* out, float* lse,
+                                             void* stream);
+
 /* Message of the last non-OK status returned on this host thread ("" if none). */
 SA_API const char* sa_last_error(void);
 
