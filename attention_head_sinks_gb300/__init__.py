@@ -11,7 +11,7 @@ from __future__ import annotations
 from ._lib import SAError, lib  # noqa: F401
 from .workloads import SINK_KEY0_BIAS, SINK_NONE, SINK_NULL_LOGIT  # noqa: F401
 
-__all__ = ["sa_varlen_window_fwd", "sa_sparse_index_fwd",
+__all__ = ["sa_varlen_window_fwd", "sa_sparse_index_fwd", "sa_block_sparse_fwd",
            "sa_sparse_index_workspace_size", "sa_device_error", "sa_version", "SAError",
            "SINK_NONE", "SINK_KEY0_BIAS", "SINK_NULL_LOGIT"]
 
@@ -126,6 +126,49 @@ def sa_sparse_index_fwd(q, kv_latent, indices, dv, sinks, sink_mode,
         indices.data_ptr(), topk, nq, hq,
         None if sinks is None else sinks.data_ptr(), int(sink_mode),
         float(softmax_scale), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes,
+        _stream_handle(stream)))
+    return out, lse
+
+
+def sa_block_sparse_fwd(q, k, v, batch, seq_len, block_table, block_size,
+                        cu_docs, sinks, sink_mode, softmax_scale, out=None,
+                        lse=None, stream=None):
+    """Block-sparse causal attention with packed documents (C:
+    ``sa_block_sparse_fwd``).
+
+    q ``[B*S,Hq,D]``, k/v ``[B*S,Hkv,D]`` bf16; block_table int32
+    ``[B*S,topk]`` (-1 padded, block ids from the batch-row start); cu_docs
+    int32 ``[num_docs+1]`` over the flattened tokens; sinks fp32 ``[Hq]`` (or
+    None with ``SINK_NONE``).  Returns ``(out, lse)``: bf16 ``[B*S,Hq,D]`` and
+    fp32 ``[Hq,B*S]``.
+    """
+    torch = _torch()
+    _dev_tensor("q", q, torch.bfloat16, 3)
+    _dev_tensor("k", k, torch.bfloat16, 3)
+    _dev_tensor("v", v, torch.bfloat16, 3)
+    _dev_tensor("block_table", block_table, torch.int32, 2)
+    _dev_tensor("cu_docs", cu_docs, torch.int32, 1)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    if T != batch * seq_len or k.shape != (T, hkv, d) or v.shape != (T, hkv, d):
+        raise ValueError("q must be [batch*seq_len, Hq, D] and k, v [batch*seq_len, Hkv, D]")
+    if block_table.shape[0] != T:
+        raise ValueError("block_table must have batch*seq_len rows")
+    if sinks is not None:
+        _dev_tensor("sinks", sinks, torch.float32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    _dev_tensor("out", out, torch.bfloat16, 3)
+    _dev_tensor("lse", lse, torch.float32, 2)
+    from ._lib import check
+    check(lib().sa_block_sparse_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), int(batch), int(seq_len), hq,
+        hkv, d, block_table.data_ptr(), block_table.shape[1], int(block_size),
+        cu_docs.data_ptr(), cu_docs.numel() - 1,
+        None if sinks is None else sinks.data_ptr(), int(sink_mode),
+        float(softmax_scale), out.data_ptr(), lse.data_ptr(), None, 0,
         _stream_handle(stream)))
     return out, lse
 

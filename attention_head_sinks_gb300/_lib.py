@@ -34,6 +34,9 @@ SIGNATURES = {
     "sa_sparse_index_fwd_noalloc": (ctypes.c_int, [
         _P, _P, _I64, _I32, _I32, _P, _I32, _I32, _I32, _P, _I32, _F32, _P, _P,
         _P]),
+    "sa_block_sparse_fwd": (ctypes.c_int, [
+        _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _I32, _P, _I32, _P,
+        _I32, _F32, _P, _P, _P, _SZ, _P]),
     "sa_last_error": (ctypes.c_char_p, []),
     "sa_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "sa_version": (ctypes.c_uint32, []),

@@ -1,0 +1,525 @@
+// block_sparse_fwd.cu -- block-sparse causal attention with packed documents
+// and a per-head NULL_LOGIT sink (DSA-style prefill).
+//
+// Operation: NeMo AutoModel "nemo_automodel.components.models.minimax_m3_vl.
+// cp_sparse_attn", MiniMaxM3CPSparseAttention step 4 -- each query attends
+// the key blocks selected for it, with token-level causality; the packed
+// document mask and the zero output of fully masked rows come from
+// _local_sparse_forward.  Key set of token i (row position p, document start
+// d): { j in i's batch row : block(j) selected by i, d <= j <= p }.  The sink
+// follows afierka-intel/vllm pull 76, Implementation (folded after the key
+// loop, LSE over real keys only).
+//
+// Tile: M = 128 rows = (128 / G) consecutive tokens x the G query heads of
+// one KV head (row = token * G + head).  Keys: the union, over the tile's
+// tokens, of their selected blocks that intersect [document start, token] --
+// built in shared memory as a bitmap over the batch row's blocks, compacted
+// to an ascending list, with a per-block bitmask of the tokens that chose it.
+// The loop walks that list two 64-key blocks per step:
+//   S_j = Q K_j^T (N = 128) into one of two TMEM buffers,
+//   softmax over S_j with per-element selection / causal / document masks,
+//   P_j (bf16) written over S_j, O += P_j V_j with P_j read from TMEM.
+// Warp roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
+// warps 4..7 softmax and epilogue (warp w reads TMEM lanes 32 (w mod 4) ...).
+// The running max is rescaled lazily: O and l are rescaled only when a row's
+// max grows by more than 2^8, so P stays below 256.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "sa_internal.h"
+#include "sa_ptx.cuh"
+
+namespace sa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kD = 128;
+constexpr int kBlk = 64;
+constexpr int kStepKeys = 128;                 // two blocks per step
+constexpr int kStages = 2;
+constexpr int kQSlab = 128 * 128;              // 128 rows x 64 dims, 16 KB
+constexpr int kKVSlab = kStepKeys * 128;       // 128 keys x 64 dims, 16 KB
+constexpr int kStageBytes = 4 * kKVSlab;       // K: 2 slabs, V: 2 slabs
+constexpr int kMaxUnion = 2048;
+constexpr int kMaxBitmapWords = 512;           // 16384 blocks per batch row
+constexpr int kTmemCols = 512;
+constexpr int kColO = 256;
+constexpr float kRescaleThreshold = 8.0f;
+
+struct BlockParams {
+  const int32_t* table;  // [T, topk]
+  int32_t topk;
+  int32_t seq_len;
+  int32_t nblocks;
+  int32_t total_tokens;
+  const int32_t* cu_docs;
+  int32_t num_docs;
+  int32_t num_q_heads;
+  const float* sinks;
+  float scale_log2;
+  __nv_bfloat16* out;  // [T, Hq, 128]
+  float* lse;          // [Hq, T]
+  uint32_t* err;
+};
+
+struct __align__(8) BlockSmemCtl {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done;
+  uint32_t tmem_base;
+  int32_t nunion;
+  int32_t tok_pos[128];  // row-local position (-1 past the last token)
+  int32_t tok_lo[128];   // row-local start of the token's document
+  uint32_t bitmap[kMaxBitmapWords];
+  int32_t prefix[kMaxBitmapWords];
+};
+
+__device__ __forceinline__ int upper_doc(const int32_t* cu, int n, int t) {
+  int lo = 0, hi = n - 1;  // largest e with cu[e] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return __ldg(cu + lo);
+}
+
+template <int G, int MODE>
+__global__ void __launch_bounds__(256, 1)
+block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const BlockParams p) {
+  constexpr int TQ = 128 / G;
+  constexpr int TW = TQ > 32 ? TQ / 32 : 1;  // token-mask words per block
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ BlockSmemCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                                  // 2 x 16 KB
+  uint8_t* sKV = sQ + 2 * kQSlab;                      // stages x 64 KB
+  int32_t* ulist = reinterpret_cast<int32_t*>(sKV + kStages * kStageBytes);
+  uint32_t* tokmask = reinterpret_cast<uint32_t*>(ulist + kMaxUnion);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.y;
+  const int tok0 = blockIdx.x * TQ;
+  const int row_start = (tok0 / p.seq_len) * p.seq_len;
+  const int nwords = (p.nblocks + 31) >> 5;
+
+  // ---- tile metadata: token positions, union of live blocks ---------------
+  if (tid < TQ) {
+    const int t = tok0 + tid;
+    if (t < p.total_tokens) {
+      ctl.tok_pos[tid] = t - row_start;
+      ctl.tok_lo[tid] = max(upper_doc(p.cu_docs, p.num_docs, t) - row_start, 0);
+    } else {
+      ctl.tok_pos[tid] = -1;
+      ctl.tok_lo[tid] = 0;
+    }
+  }
+  for (int w = tid; w < nwords; w += 256) ctl.bitmap[w] = 0u;
+  if (tid == 0) {
+    mbar_init(&ctl.q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl.kv_full[s], 1);
+      mbar_init(&ctl.kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl.s_full[b], 1);
+      mbar_init(&ctl.p_full[b], 4);
+    }
+    mbar_init(&ctl.o_done, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int npairs = TQ * p.topk;
+  for (int w = tid; w < npairs; w += 256) {
+    const int i = w / p.topk;
+    const int pos = ctl.tok_pos[i];
+    if (pos < 0) continue;
+    const int b = __ldg(p.table + (int64_t)(tok0 + i) * p.topk + (w - i * p.topk));
+    if (b >= 0 && b < p.nblocks && b * kBlk <= pos && b * kBlk + kBlk - 1 >= ctl.tok_lo[i])
+      atomicOr(&ctl.bitmap[b >> 5], 1u << (b & 31));
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive prefix of popcounts over the bitmap words
+    const int per = (nwords + 31) >> 5;
+    int local = 0;
+    for (int k = 0; k < per; ++k) {
+      const int w = lane * per + k;
+      if (w < nwords) local += __popc(ctl.bitmap[w]);
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int k = 0; k < per; ++k) {
+      const int w = lane * per + k;
+      if (w < nwords) {
+        ctl.prefix[w] = run;
+        run += __popc(ctl.bitmap[w]);
+      }
+    }
+    if (lane == 31) ctl.nunion = incl;
+  }
+  __syncthreads();
+  const int U = ctl.nunion;
+  for (int w = tid; w < nwords; w += 256) {
+    uint32_t bits = ctl.bitmap[w];
+    int o = ctl.prefix[w];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      ulist[o++] = w * 32 + b;
+    }
+  }
+  for (int w = tid; w < U * TW; w += 256) tokmask[w] = 0u;
+  __syncthreads();
+  for (int w = tid; w < npairs; w += 256) {
+    const int i = w / p.topk;
+    const int pos = ctl.tok_pos[i];
+    if (pos < 0) continue;
+    const int b = __ldg(p.table + (int64_t)(tok0 + i) * p.topk + (w - i * p.topk));
+    if (b >= 0 && b < p.nblocks && b * kBlk <= pos && b * kBlk + kBlk - 1 >= ctl.tok_lo[i]) {
+      const uint32_t word = ctl.bitmap[b >> 5];
+      const int u = ctl.prefix[b >> 5] + __popc(word & ((1u << (b & 31)) - 1u));
+      atomicOr(&tokmask[u * TW + (i >> 5)], 1u << (i & 31));
+    }
+  }
+  if (warp == 2) {
+    tmem_alloc(&ctl.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const int nsteps = (U + 1) >> 1;
+  bool ok = true;
+
+  if (tid == 0 && nsteps > 0) {
+    // ---- producer ------------------------------------------------------------
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+    mbar_arrive_expect_tx(&ctl.q_full, 2 * kQSlab);
+    for (int s = 0; s < 2; ++s)
+      tma_load_3d(sQ + s * kQSlab, &tm_q, &ctl.q_full, 64 * s, g * G, tok0);
+    int issued = 0;
+    for (int j = 0; j < nsteps; ++j) {
+      const int st = j & 1;
+      if (j >= kStages) {
+        ok = mbar_wait(&ctl.kv_empty[st], ((j >> 1) - 1) & 1, p.err, kErrWaitFree);
+        if (!ok) break;
+      }
+      const int nb = min(2, U - 2 * j);
+      uint8_t* stage = sKV + st * kStageBytes;
+      mbar_arrive_expect_tx(&ctl.kv_full[st], (uint32_t)nb * 4u * (kBlk * 128));
+      for (int bi = 0; bi < nb; ++bi) {
+        const int kpos = row_start + ulist[2 * j + bi] * kBlk;
+        for (int s = 0; s < 2; ++s) {
+          tma_load_3d(stage + s * kKVSlab + bi * (kBlk * 128), &tm_k, &ctl.kv_full[st],
+                      64 * s, g, kpos);
+          tma_load_3d(stage + (2 + s) * kKVSlab + bi * (kBlk * 128), &tm_v, &ctl.kv_full[st],
+                      64 * s, g, kpos);
+        }
+      }
+      issued = j + 1;
+    }
+    if (!ok) {
+      // bounded drain of the copies still in flight
+      for (int j = max(0, issued - kStages); j < issued; ++j)
+        mbar_wait(&ctl.kv_full[j & 1], (j >> 1) & 1, p.err, kErrWaitDrain);
+    }
+  } else if (tid == 32 && nsteps > 0) {
+    // ---- MMA issuer ----------------------------------------------------------
+    ok = mbar_wait(&ctl.q_full, 0, p.err, kErrWaitLoad);
+    auto issue_s = [&](int j) -> bool {
+      const int st = j & 1;
+      if (!mbar_wait(&ctl.kv_full[st], (j >> 1) & 1, p.err, kErrWaitLoad)) return false;
+      tc_fence_after();
+      const int nb = min(2, U - 2 * j);
+      const uint32_t idesc = idesc_bf16(128, nb * kBlk, false);
+      const uint8_t* kst = sKV + st * kStageBytes;
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t a = smem_desc(smem_u32(sQ + s * kQSlab) + kk * 32, 16, 1024, kLayoutSw128);
+          const uint64_t b = smem_desc(smem_u32(kst + s * kKVSlab) + kk * 32, 16, 1024, kLayoutSw128);
+          mma_ss(tmem + (uint32_t)(st * 128), a, b, idesc, (s | kk) ? 1u : 0u);
+        }
+      }
+      mma_commit(&ctl.s_full[st]);
+      return true;
+    };
+    if (ok) ok = issue_s(0);
+    for (int j = 0; j < nsteps && ok; ++j) {
+      if (j + 1 < nsteps) {
+        ok = issue_s(j + 1);
+        if (!ok) break;
+      }
+      const int st = j & 1;
+      ok = mbar_wait(&ctl.p_full[st], (j >> 1) & 1, p.err, kErrWaitMma);
+      if (!ok) break;
+      tc_fence_after();
+      const int nb = min(2, U - 2 * j);
+      const uint32_t idesc = idesc_bf16(128, kD, true);
+      const uint8_t* vst = sKV + st * kStageBytes + 2 * kKVSlab;
+      for (int kk = 0; kk < nb * kBlk / 16; ++kk) {
+        const uint64_t b = smem_desc(smem_u32(vst) + kk * 16 * 128, kKVSlab, 1024, kLayoutSw128);
+        mma_ts(tmem + kColO, tmem + (uint32_t)(st * 128) + kk * 8, b, idesc,
+               (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(&ctl.kv_empty[st]);
+      mma_commit(&ctl.o_done);
+    }
+  } else if (warp >= 4) {
+    // ---- softmax + epilogue (thread = row = TMEM lane) -----------------------
+    const int row = (warp - 4) * 32 + lane;
+    const int tok = row / G;
+    const int h = g * G + (row % G);
+    const int t = tok0 + tok;
+    const int pos = ctl.tok_pos[tok];
+    const int dlo = ctl.tok_lo[tok];
+    const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    const float c2 = p.scale_log2;
+    float m_use = -INFINITY, l = 0.f;
+
+    for (int j = 0; j < nsteps; ++j) {
+      const int st = j & 1;
+      ok = mbar_wait(&ctl.s_full[st], (j >> 1) & 1, p.err, kErrWaitMma);
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const int nb = min(2, U - 2 * j);
+      // live column range per block: [clo, chi] (empty -> unreachable range)
+      int clo[2], chi[2];
+#pragma unroll
+      for (int bi = 0; bi < 2; ++bi) {
+        clo[bi] = 1 << 30;
+        chi[bi] = 1 << 30;
+        if (bi < nb && pos >= 0) {
+          const int u = 2 * j + bi;
+          if ((tokmask[u * TW + (tok >> 5)] >> (tok & 31)) & 1u) {
+            const int bs = ulist[u] * kBlk;
+            clo[bi] = max(dlo, bs) - bs;
+            chi[bi] = min(pos, bs + kBlk - 1) - bs;
+          }
+        }
+      }
+      const uint32_t sbase = lane_base + (uint32_t)(st * 128);
+      // pass 1: step max
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int bi = c >> 1;
+        const int c0 = (c & 1) * 32;
+        float s[32];
+        tmem_ld32(sbase + 32 * c, s);
+        tmem_wait_ld();
+        const uint32_t span = (uint32_t)(chi[bi] - clo[bi]);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          mx = fmaxf(mx, ((uint32_t)(c0 + e - clo[bi]) <= span) ? s[e] * c2 : -INFINITY);
+      }
+      // lazy rescale of O and l when this row's max grew by more than 2^8
+      const bool need = mx > m_use + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mx : m_use;
+        const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
+        if (j > 0) {
+          ok = mbar_wait(&ctl.o_done, (j - 1) & 1, p.err, kErrWaitMma);
+          __syncwarp();
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < kD / 32; ++c) {
+            float o[32];
+            tmem_ld32(lane_base + kColO + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(lane_base + kColO + 32 * c, o);
+          }
+          tmem_wait_st();
+          l *= alpha;
+        }
+        m_use = m_new;
+      }
+      const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;
+      // pass 2: P = 2^(x - m) (bf16, in place), row sum
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int bi = c >> 1;
+        const int c0 = (c & 1) * 32;
+        float s[32];
+        tmem_ld32(sbase + 32 * c, s);
+        tmem_wait_ld();
+        const uint32_t span = (uint32_t)(chi[bi] - clo[bi]);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          s[e] = ((uint32_t)(c0 + e - clo[bi]) <= span) ? ex2_approx(fmaf(s[e], c2, -m_ref)) : 0.f;
+          l += s[e];
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(s[2 * e], s[2 * e + 1]);
+        tmem_st16(sbase + 16 * c, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.p_full[st]);
+    }
+    if (ok && nsteps > 0) {
+      ok = mbar_wait(&ctl.o_done, (nsteps - 1) & 1, p.err, kErrWaitMma);
+      __syncwarp();
+      tc_fence_after();
+    }
+    // epilogue
+    float inv = 0.f, lse = -INFINITY;
+    if (m_use != -INFINITY) {
+      float den = l, alpha = 1.f;
+      if (MODE == SA_SINK_NULL_LOGIT) {
+        const float sink2 = __ldg(p.sinks + h) * kLog2e;
+        const float mp = fmaxf(m_use, sink2);
+        alpha = ex2_approx(m_use - mp);
+        den = l * alpha + ex2_approx(sink2 - mp);
+      }
+      inv = alpha / den;
+      lse = (m_use + log2f(l)) * kLn2;
+    }
+    const bool row_valid = pos >= 0;
+    __nv_bfloat16* orow = p.out + ((int64_t)t * p.num_q_heads + h) * kD;
+#pragma unroll 1
+    for (int jj = 0; jj < kD / 16; ++jj) {
+      float o[16];
+      if (nsteps > 0) {
+        tmem_ld16(lane_base + kColO + 16 * jj, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[e] = 0.f;
+      }
+      if (row_valid) {
+        uint4 w0, w1;
+        w0.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+        w0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+        w0.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+        w0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+        w1.x = pack_bf16x2(o[8] * inv, o[9] * inv);
+        w1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
+        w1.z = pack_bf16x2(o[12] * inv, o[13] * inv);
+        w1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
+        uint4* dst = reinterpret_cast<uint4*>(orow + 16 * jj);
+        dst[0] = w0;
+        dst[1] = w1;
+      }
+    }
+    if (row_valid) p.lse[(int64_t)h * p.total_tokens + t] = lse;
+  }
+
+  // ---- teardown ----------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int G, int MODE>
+sa_status launch_typed(const BlockArgs& a) {
+  constexpr int TQ = 128 / G;
+  constexpr int TW = TQ > 32 ? TQ / 32 : 1;
+  const int64_t T = (int64_t)a.batch * a.seq_len;
+  CUtensorMap tq, tk, tv;
+  const uint64_t dq[3] = {(uint64_t)kD, (uint64_t)a.num_q_heads, (uint64_t)T};
+  const uint64_t sq[2] = {(uint64_t)kD * 2, (uint64_t)a.num_q_heads * kD * 2};
+  const uint32_t bq[3] = {64, (uint32_t)G, (uint32_t)TQ};
+  const uint64_t dk[3] = {(uint64_t)kD, (uint64_t)a.num_kv_heads, (uint64_t)T};
+  const uint64_t sk[2] = {(uint64_t)kD * 2, (uint64_t)a.num_kv_heads * kD * 2};
+  const uint32_t bk[3] = {64, 1, (uint32_t)kBlk};
+  if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dq, sq, bq,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dk, sk, bk,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dk, sk, bk,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return SA_ERR_INVALID_ARG;
+  BlockParams p;
+  p.table = a.block_table;
+  p.topk = a.topk_blocks;
+  p.seq_len = a.seq_len;
+  p.nblocks = a.seq_len / kBlk;
+  p.total_tokens = (int32_t)T;
+  p.cu_docs = a.cu_docs;
+  p.num_docs = a.num_docs;
+  p.num_q_heads = a.num_q_heads;
+  p.sinks = a.sinks;
+  p.scale_log2 = a.softmax_scale * kLog2e;
+  p.out = reinterpret_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.err = device_error_word();
+  const size_t smem = 1024 + 2 * kQSlab + (size_t)kStages * kStageBytes +
+                      (size_t)kMaxUnion * 4 + (size_t)kMaxUnion * TW * 4;
+  auto kern = block_sparse_fwd_kernel<G, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess)
+    return fail(SA_ERR_CUDA, "sa_block_sparse_fwd: %s", cudaGetErrorString(e));
+  dim3 grid((unsigned)(T / TQ), (unsigned)a.num_kv_heads);
+  kern<<<grid, 256, smem, a.stream>>>(tq, tk, tv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return fail(SA_ERR_CUDA, "sa_block_sparse_fwd launch: %s", cudaGetErrorString(e));
+  return SA_OK;
+}
+
+template <int G>
+sa_status by_mode(const BlockArgs& a) {
+  if (a.sink_mode == SA_SINK_NULL_LOGIT) return launch_typed<G, SA_SINK_NULL_LOGIT>(a);
+  return launch_typed<G, SA_SINK_NONE>(a);
+}
+
+}  // namespace
+
+sa_status launch_block_sparse_fwd(const BlockArgs& a) {
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const char* fn = "sa_block_sparse_fwd";
+  if (a.head_dim != kD)
+    return fail(SA_ERR_UNSUPPORTED, "%s: head_dim %d (supported: 128)", fn, a.head_dim);
+  if (a.block_size != kBlk)
+    return fail(SA_ERR_UNSUPPORTED, "%s: block_size %d (supported: 64)", fn, a.block_size);
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+    return fail(SA_ERR_UNSUPPORTED,
+                "%s: num_q_heads / num_kv_heads = %d (supported: 1, 2, 4, 8, 16)", fn, G);
+  if (a.seq_len % 128 != 0)
+    return fail(SA_ERR_UNSUPPORTED, "%s: seq_len %d is not a multiple of 128", fn, a.seq_len);
+  if (a.seq_len / kBlk > kMaxBitmapWords * 32)
+    return fail(SA_ERR_UNSUPPORTED, "%s: seq_len %d above %d", fn, a.seq_len,
+                kMaxBitmapWords * 32 * kBlk);
+  if ((128 / G) * a.topk_blocks > kMaxUnion)
+    return fail(SA_ERR_UNSUPPORTED,
+                "%s: %d tokens per tile x topk_blocks %d above %d selections per tile", fn,
+                128 / G, a.topk_blocks, kMaxUnion);
+  switch (G) {
+    case 1: return by_mode<1>(a);
+    case 2: return by_mode<2>(a);
+    case 4: return by_mode<4>(a);
+    case 8: return by_mode<8>(a);
+    default: return by_mode<16>(a);
+  }
+}
+
+}  // namespace sa

@@ -177,6 +177,68 @@ sa_status sa_varlen_window_fwd(const void* q, const void* k, const void* v,
   return sa::launch_window_fwd(a);
 }
 
+sa_status sa_block_sparse_fwd(const void* q, const void* k, const void* v, int32_t batch,
+                              int32_t seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, const int32_t* block_table,
+                              int32_t topk_blocks, int32_t block_size,
+                              const int32_t* cu_docs, int32_t num_docs, const float* sinks,
+                              int32_t sink_mode, float softmax_scale, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  const char* fn = "sa_block_sparse_fwd";
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!q || !k || !v || !cu_docs || !out || !lse || (topk_blocks > 0 && !block_table))
+    return fail(SA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (sink_mode < SA_SINK_NONE || sink_mode > SA_SINK_NULL_LOGIT)
+    return fail(SA_ERR_INVALID_ARG, "%s: unknown sink_mode %d", fn, sink_mode);
+  if (sink_mode != SA_SINK_NONE && !sinks)
+    return fail(SA_ERR_INVALID_ARG, "%s: sinks is NULL with sink_mode %d", fn, sink_mode);
+  if (batch < 0 || seq_len < 0 || topk_blocks < 0 || block_size < 1 || num_docs < 1 ||
+      head_dim < 1)
+    return fail(SA_ERR_INVALID_ARG,
+                "%s: bad sizes (batch %d, seq_len %d, topk_blocks %d, block_size %d, "
+                "num_docs %d, head_dim %d)",
+                fn, batch, seq_len, topk_blocks, block_size, num_docs, head_dim);
+  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0)
+    return fail(SA_ERR_INVALID_ARG,
+                "%s: num_q_heads %d must be a positive multiple of num_kv_heads %d", fn,
+                num_q_heads, num_kv_heads);
+  if ((int64_t)batch * seq_len >= ((int64_t)1 << 31))
+    return fail(SA_ERR_INVALID_ARG, "%s: batch * seq_len >= 2^31", fn);
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale))
+    return fail(SA_ERR_INVALID_ARG, "%s: softmax_scale must be finite and > 0", fn);
+  if (!sa::aligned(q, 16) || !sa::aligned(k, 16) || !sa::aligned(v, 16) ||
+      !sa::aligned(out, 16) || !sa::aligned(lse, 4) || !sa::aligned(cu_docs, 4) ||
+      (block_table && !sa::aligned(block_table, 4)) || (sinks && !sa::aligned(sinks, 4)))
+    return fail(SA_ERR_INVALID_ARG, "%s: misaligned pointer (bf16 tensors need 16 bytes)", fn);
+  if (sink_mode == SA_SINK_KEY0_BIAS)
+    return fail(SA_ERR_UNSUPPORTED, "%s: KEY0_BIAS is not supported on the block path", fn);
+  if ((int64_t)batch * seq_len == 0) return SA_OK;
+  if (!sa::device_error_word())
+    return fail(SA_ERR_CUDA, "%s: no usable CUDA device", fn);
+  sa::BlockArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.batch = batch;
+  a.seq_len = seq_len;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_table = block_table;
+  a.topk_blocks = topk_blocks;
+  a.block_size = block_size;
+  a.cu_docs = cu_docs;
+  a.num_docs = num_docs;
+  a.sinks = sinks;
+  a.sink_mode = sink_mode;
+  a.softmax_scale = softmax_scale;
+  a.out = out;
+  a.lse = lse;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return sa::launch_block_sparse_fwd(a);
+}
+
 size_t sa_sparse_index_workspace_size(int32_t num_queries, int32_t num_q_heads,
                                       int32_t dv, int32_t topk) {
   if (num_queries <= 0 || num_q_heads <= 0 || dv != 512 || topk <= 0) return 0;

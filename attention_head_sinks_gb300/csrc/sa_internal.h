@@ -69,4 +69,28 @@ size_t sparse_index_workspace_bytes(int32_t num_queries, int32_t num_q_heads, in
 int sparse_index_max_topk();
 sa_status launch_sparse_index_fwd(const IndexArgs& a);
 
+struct BlockArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int32_t batch;
+  int32_t seq_len;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  const int32_t* block_table;
+  int32_t topk_blocks;
+  int32_t block_size;
+  const int32_t* cu_docs;
+  int32_t num_docs;
+  const float* sinks;
+  int32_t sink_mode;
+  float softmax_scale;
+  void* out;
+  float* lse;
+  cudaStream_t stream;
+};
+
+sa_status launch_block_sparse_fwd(const BlockArgs& a);
+
 }  // namespace sa

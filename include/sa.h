@@ -139,6 +139,45 @@ SA_API size_t sa_sparse_index_workspace_size(int32_t num_queries,
                                              int32_t topk);
 
 /*
+ * Block-sparse causal attention with packed documents (DSA-style prefill) --
+ * the sparse attention of NeMo AutoModel "nemo_automodel.components.models.
+ * minimax_m3_vl.cp_sparse_attn" (MiniMaxM3CPSparseAttention step 4: selected
+ * key blocks + token-level causal; _local_sparse_forward: packed document
+ * masks, zero output for fully masked rows).  Tokens are batch rows of
+ * seq_len packed back to back.  Key set of token i at row position p whose
+ * document starts at row position d:
+ *   { j in i's batch row : (j's row position) / block_size listed in
+ *     block_table[i, :],  d <= j's row position <= p }.
+ * Block ids count blocks from the start of the batch row; ids outside
+ * [0, seq_len / block_size) (the -1 padding) are absent; a repeated id is one
+ * selection.  One selection per token is shared by all heads.  A row with an
+ * empty key set gives zero output and LSE = -inf.  NONE and NULL_LOGIT are
+ * supported; KEY0_BIAS returns SA_ERR_UNSUPPORTED.
+ *
+ *   q            bf16 [batch * seq_len, num_q_heads, head_dim]
+ *   k, v         bf16 [batch * seq_len, num_kv_heads, head_dim]
+ *   block_table  int32 [batch * seq_len, topk_blocks]
+ *   cu_docs      int32 [num_docs + 1]: document starts over the flattened
+ *                tokens, cu_docs[0] = 0, non-decreasing, last = batch*seq_len
+ *   out          bf16 [batch * seq_len, num_q_heads, head_dim]   (written)
+ *   lse          fp32 [num_q_heads, batch * seq_len]              (written)
+ *   workspace    reserved: the current kernel needs none (NULL / 0 accepted)
+ * Supported: head_dim = 128, block_size = 64, num_q_heads / num_kv_heads in
+ * {1, 2, 4, 8, 16}, seq_len a multiple of 128 and <= 1048576,
+ * (128 / that ratio) * topk_blocks <= 2048, batch * seq_len < 2^31.
+ */
+SA_API sa_status sa_block_sparse_fwd(const void* q, const void* k, const void* v,
+                                     int32_t batch, int32_t seq_len,
+                                     int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, const int32_t* block_table,
+                                     int32_t topk_blocks, int32_t block_size,
+                                     const int32_t* cu_docs, int32_t num_docs,
+                                     const float* sinks, int32_t sink_mode,
+                                     float softmax_scale, void* out, float* lse,
+                                     void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
  * Allocation-free variant of sa_sparse_index_fwd.  The pages have no
  * counterpart: it exists for callers that cannot allocate device memory for a
  * workspace -- for example code running inside a host runtime that owns the

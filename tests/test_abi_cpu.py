@@ -125,3 +125,34 @@ def test_sparse_index_workspace_size(lib):
 
 def test_sparse_index_empty_batch_is_a_no_op(lib):
     assert _index_call(lib, nq=0) == 0
+
+
+def _block_call(lib, **kw):
+    a = dict(q=16, k=16, v=16, batch=2, S=8192, hq=32, hkv=4, d=128, tab=16, topk=16,
+             bs=64, cu=16, ndocs=6, sinks=16, mode=2, scale=0.08, out=16, lse=16)
+    a.update(kw)
+    return lib.sa_block_sparse_fwd(
+        a["q"], a["k"], a["v"], a["batch"], a["S"], a["hq"], a["hkv"], a["d"], a["tab"],
+        a["topk"], a["bs"], a["cu"], a["ndocs"], a["sinks"], a["mode"], a["scale"],
+        a["out"], a["lse"], None, 0, None)
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(q=None), 1, "NULL"),
+    (dict(tab=None), 1, "NULL"),
+    (dict(mode=3), 1, "sink_mode"),
+    (dict(sinks=None), 1, "sinks is NULL"),
+    (dict(ndocs=0), 1, "bad sizes"),
+    (dict(bs=0), 1, "bad sizes"),
+    (dict(hq=30), 1, "multiple"),
+    (dict(batch=1 << 20), 1, "2^31"),
+    (dict(out=8), 1, "misaligned"),
+    (dict(mode=1), 2, "KEY0_BIAS"),
+])
+def test_block_sparse_rejects_bad_arguments(lib, kw, status, needle):
+    assert _block_call(lib, **kw) == status
+    assert needle in lib.sa_last_error().decode()
+
+
+def test_block_sparse_empty_batch_is_a_no_op(lib):
+    assert _block_call(lib, batch=0) == 0
