@@ -59,7 +59,7 @@ sa_status fail(sa_status st, const char* fmt, ...) {
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank,
                   const void* base, const uint64_t* dims,
                   const uint64_t* strides_bytes, const uint32_t* box,
-                  CUtensorMapSwizzle swizzle) {
+                  CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promotion) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable (no CUDA driver?)");
@@ -71,8 +71,7 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank,
                   reinterpret_cast<const cuuint64_t*>(strides_bytes),
                   reinterpret_cast<const cuuint32_t*>(box), estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  promotion, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     fail(SA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return false;
@@ -91,6 +90,18 @@ uint32_t* device_error_word() {
   p = static_cast<uint32_t*>(addr);
   g_err_ptr[dev].store(p, std::memory_order_release);
   return p;
+}
+
+int num_sms() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
+    v = 1;
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
 }
 
 }  // namespace sa

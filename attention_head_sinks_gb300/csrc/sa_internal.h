@@ -15,10 +15,14 @@ sa_status fail(sa_status st, const char* fmt, ...);
 
 // Encodes a tiled TMA descriptor through the driver entry point (no libcuda
 // link dependency).  Returns false with a message on failure.
+// `promotion` is the L2 fetch granularity for the map's misses: rows that are
+// narrower than it and strided apart (one head of a token) want NONE, or the
+// L2 pulls bytes of neighbouring heads that may be evicted before use.
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank,
                   const void* base, const uint64_t* dims,
                   const uint64_t* strides_bytes, const uint32_t* box,
-                  CUtensorMapSwizzle swizzle);
+                  CUtensorMapSwizzle swizzle,
+                  CUtensorMapL2promotion promotion = CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 
 // Address of this device's error word (a __device__ variable).
 uint32_t* device_error_word();
@@ -44,6 +48,14 @@ struct WindowArgs {
 };
 
 sa_status launch_window_fwd(const WindowArgs& a);
+
+// Persistent ring kernel for the window path.  Returns false (launching
+// nothing) when the shape does not fit it; otherwise launches and stores the
+// launch status in *st.
+bool launch_window_ring(const WindowArgs& a, sa_status* st);
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
 
 struct IndexArgs {
   const void* q;

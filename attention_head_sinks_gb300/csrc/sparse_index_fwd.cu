@@ -481,7 +481,7 @@ sa_status launch_typed(const IndexArgs& a, int nslices) {
   if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, dq, sq, bq,
                     CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tiled(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kv, dk, sq, bk,
-                    CU_TENSOR_MAP_SWIZZLE_128B))
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
     return SA_ERR_INVALID_ARG;
   IndexParams p;
   p.indices = a.indices;

@@ -29,12 +29,12 @@
 
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
+#include "window_common.cuh"
 
 namespace sa {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
+using win::kLog2e;
 constexpr int kTmemCols = 256;
 constexpr int kColS = 0;
 constexpr int kColP = 0;
@@ -61,16 +61,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
       (reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Largest b with cu[b] <= t (0 <= b < n), i.e. the sequence holding token t.
-__device__ __forceinline__ int find_seq(const int32_t* cu, int n, int t) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 template <int D, int G, int MODE>
 __global__ void __launch_bounds__(128, 1)
 window_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -79,6 +69,7 @@ window_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const WindowParams p) {
   constexpr int TQ = 128 / G;
   constexpr int NSLAB = D / 16;
+  static_assert(TQ * G == 128, "tile rows");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_load, bar_s, bar_o;
   __shared__ uint32_t tmem_base_sh;
@@ -141,105 +132,21 @@ window_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   // ---- per-row metadata -------------------------------------------------
   const int row = warp * 32 + lane;  // TMEM lane == M row
-  const int tl = row / G;
-  const int h = g * G + (row % G);
-  const int t = tok0 + tl;
-  const bool row_valid = t < p.total_tokens;
-  // Live key columns [clo, chi] and the key-0 column; rows past the end of
-  // the tokens get a range no column reaches.
-  int clo = 1 << 30, chi = 1 << 30, ck0 = -1;
-  if (row_valid) {
-    const int b = find_seq(p.cu_seqlens, p.num_seqs, t);
-    const int s0 = __ldg(p.cu_seqlens + b);
-    const int s1 = __ldg(p.cu_seqlens + b + 1);
-    const int lo = max(s0, t - p.wl);
-    const int hi = min(s1 - 1, t + p.wr);
-    clo = lo - kstart;
-    chi = hi - kstart;
-    if (MODE == SA_SINK_KEY0_BIAS && s0 >= lo) ck0 = s0 - kstart;
-  }
-  const float sink = (MODE != SA_SINK_NONE) ? __ldg(p.sinks + h) : 0.f;
-  const float sink2 = sink * kLog2e;
-  const float c2 = p.scale_log2;
-
+  const win::RowMeta r = win::row_meta<G, MODE>(p.cu_seqlens, p.num_seqs, p.total_tokens,
+                                                 row, g, tok0, kstart, p.wl, p.wr, p.sinks);
   // Columns any row of this warp can see (before sequence clipping).
   const int wc_lo = (warp * 32) / G;
   const int wc_hi = min((warp * 32 + 31) / G + p.wl + p.wr, nk - 1);
-  const int ch_lo = wc_lo >> 5;
-  const int ch_hi = wc_hi >> 5;
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
 
   bool s_ok = mbar_wait(&bar_s, 0, p.err, kErrWaitMma);
   __syncwarp();
   tc_fence_after();
 
-  // ---- pass 1: row max of the scaled (log2) logits ------------------------
-  float m = -INFINITY;
-  for (int c = ch_lo; c <= ch_hi; ++c) {
-    float s[32];
-    tmem_ld32(lane_base + kColS + 32 * c, s);
-    tmem_wait_ld();
-    const int c0 = 32 * c;
-    const bool full = __all_sync(0xffffffffu, c0 >= clo && c0 + 31 <= chi);
-    const bool has_k0 = (MODE == SA_SINK_KEY0_BIAS) &&
-                        __any_sync(0xffffffffu, ck0 >= c0 && ck0 < c0 + 32);
-    if (full) {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) s[e] = s[e] * c2;
-    } else {
-      const uint32_t span = (uint32_t)(chi - clo);
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        s[e] = ((uint32_t)(c0 + e - clo) <= span) ? s[e] * c2 : -INFINITY;
-    }
-    if (has_k0) {
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (c0 + e == ck0) s[e] = s[e] + sink2;
-    }
-#pragma unroll
-    for (int e = 0; e < 32; ++e) m = fmaxf(m, s[e]);
-  }
-  // Rows with no finite logit use 0 as the reference so that -inf - m stays -inf.
-  const float m_use = (m == -INFINITY) ? 0.f : m;
-
-  // ---- pass 2: P = 2^(x - m) as bf16 into TMEM, row sum -------------------
-  float l = 0.f;
-  for (int c = 0; c < nk / 32; ++c) {
-    uint32_t pk[16];
-    if (c >= ch_lo && c <= ch_hi) {
-      float s[32];
-      tmem_ld32(lane_base + kColS + 32 * c, s);
-      tmem_wait_ld();
-      const int c0 = 32 * c;
-      const bool full = __all_sync(0xffffffffu, c0 >= clo && c0 + 31 <= chi);
-      const bool has_k0 = (MODE == SA_SINK_KEY0_BIAS) &&
-                          __any_sync(0xffffffffu, ck0 >= c0 && ck0 < c0 + 32);
-      // Every branch forms the exponent as fma(s, c2, -m) (+ sink on key 0)
-      // so that a zero KEY0_BIAS sink reproduces the no-sink bits exactly.
-      if (full && !has_k0) {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s[e] = ex2_approx(fmaf(s[e], c2, -m_use));
-      } else {
-        const uint32_t span = (uint32_t)(chi - clo);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = fmaf(s[e], c2, -m_use);
-          if (MODE == SA_SINK_KEY0_BIAS && c0 + e == ck0) x = x + sink2;
-          s[e] = ((uint32_t)(c0 + e - clo) <= span) ? ex2_approx(x) : 0.f;
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 32; ++e) l += s[e];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(s[2 * e], s[2 * e + 1]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) pk[e] = 0u;
-    }
-    tmem_st16(lane_base + kColP + 16 * c, pk);
-  }
-  tmem_wait_st();
+  // ---- softmax: P = 2^(x - m) as bf16 into TMEM, row max and sum ----------
+  float m, l;
+  win::softmax_rows<MODE>(lane_base + kColS, lane_base + kColP, nk / 32, wc_lo >> 5,
+                          wc_hi >> 5, r, p.scale_log2, m, l);
   tc_fence_before();
   __syncthreads();
 
@@ -263,39 +170,8 @@ window_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   tc_fence_after();
 
   // ---- epilogue: sink fold, normalise, store O (bf16) and LSE (fp32) ------
-  float inv = 0.f, lse = -INFINITY;
-  if (m != -INFINITY) {
-    float den = l, alpha = 1.f;
-    if (MODE == SA_SINK_NULL_LOGIT) {
-      const float mp = fmaxf(m, sink2);
-      alpha = ex2_approx(m - mp);
-      den = l * alpha + ex2_approx(sink2 - mp);
-    }
-    inv = alpha / den;
-    lse = (m + log2f(l)) * kLn2;
-  }
-  __nv_bfloat16* orow = p.out + ((int64_t)t * p.num_q_heads + h) * D;
-#pragma unroll
-  for (int j = 0; j < NSLAB; ++j) {
-    float o[16];
-    tmem_ld16(lane_base + kColO + 16 * j, o);
-    tmem_wait_ld();
-    if (row_valid) {
-      uint4 w0, w1;
-      w0.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-      w0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-      w0.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-      w0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-      w1.x = pack_bf16x2(o[8] * inv, o[9] * inv);
-      w1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
-      w1.z = pack_bf16x2(o[12] * inv, o[13] * inv);
-      w1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
-      uint4* dst = reinterpret_cast<uint4*>(orow + 16 * j);
-      dst[0] = w0;
-      dst[1] = w1;
-    }
-  }
-  if (row_valid) p.lse[(int64_t)h * p.total_tokens + t] = lse;
+  win::epilogue_row<D, MODE>(lane_base + kColO, r, m, l, p.out, p.lse, p.num_q_heads,
+                             p.total_tokens);
 
   // ---- teardown ------------------------------------------------------------
   if (threadIdx.x == 0 && !load_ok) {
@@ -323,11 +199,11 @@ sa_status launch_typed(const WindowArgs& a, int nk) {
   const uint64_t sk[2] = {(uint64_t)D * 2, (uint64_t)a.num_kv_heads * D * 2};
   const uint32_t bk[3] = {16, 1, (uint32_t)nk};
   if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dq, sq, bq,
-                    CU_TENSOR_MAP_SWIZZLE_32B) ||
+                    CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
       !encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dk, sk, bk,
-                    CU_TENSOR_MAP_SWIZZLE_32B) ||
+                    CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
       !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dk, sk, bk,
-                    CU_TENSOR_MAP_SWIZZLE_32B))
+                    CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return SA_ERR_INVALID_ARG;
 
   WindowParams p;
@@ -387,6 +263,10 @@ sa_status launch_window_fwd(const WindowArgs& a) {
   if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
     return fail(SA_ERR_UNSUPPORTED,
                 "sa_varlen_window_fwd: num_q_heads / num_kv_heads = %d (supported: 1, 2, 4, 8, 16)", G);
+  if (a.head_dim == 64 || a.head_dim == 80 || a.head_dim == 128) {
+    sa_status st = SA_OK;
+    if (launch_window_ring(a, &st)) return st;
+  }
   const int TQ = 128 / G;
   const int span = TQ + a.window_left + a.window_right;
   const int nk = (span + 31) / 32 * 32;

@@ -5,16 +5,22 @@ Default workload: the vision-tower window block at 16384 tokens (4 packed
 sequences of 4096), 16 MHA heads, head dim 80, symmetric window 64, KEY0_BIAS
 sinks -- the window-attention call whose H100 cost the MiMo sinks pull
 request quotes.  One step = one call of the C-ABI entry point (all of the
-forward runs inside its kernel).  Prints ONE JSON line on rank 0.
+forward runs inside its kernels).  Prints ONE JSON line on rank 0.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the CPU oracle as the reference arm
 
+Other workloads (--workload): the 4096-token vision block, the 16384-token
+GQA window, the sparse MLA decode (64 queries x 128 heads, top-2048 indices,
+NULL_LOGIT) and the block-sparse DSA prefill (2 x 8192 tokens, top-16
+blocks, NULL_LOGIT).
+
 Timing: W untimed warm-up calls, then K calls bracketed by a barrier and
 torch.cuda.synchronize(); each call is also bracketed by CUDA events on the
-launching stream for the kernel's own duration.  Several input sets rotate so
-that the inputs touched between two calls exceed the 129 MB L2.  SM clocks and
-throttle reasons are sampled with nvidia-smi during the timed region.
+launching stream for its kernels' duration.  Several input sets rotate so that
+the bytes touched between two calls of one set exceed the 129 MB L2.  SM
+clocks and throttle reasons are sampled with nvidia-smi during the timed
+region.
 """
 from __future__ import annotations
 
@@ -37,8 +43,9 @@ from attention_head_sinks_gb300 import workloads as W  # noqa: E402
 
 MODE_NAMES = {0: "NONE", 1: "KEY0_BIAS", 2: "NULL_LOGIT"}
 L2_BYTES = 129 * 1024 * 1024
-# The pages' cost of the same call on H100 (FA varlen + post-hoc key-0 sink
-# correction, 16384 tokens, 16 heads, head dim 80, window 64): 0.289 ms.
+METRIC = "attn fwd us/call (achieved HBM GB/s as % of GB300 roofline)"
+# The pages' cost of the same window call on H100 (FA varlen + post-hoc key-0
+# sink correction, 16 heads, head dim 80, window 64).
 PAGES_H100_US = {"vision_window_16384tok": 289.0, "vision_window_4096tok": 248.0}
 
 
@@ -46,110 +53,281 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+def _torch_bits(a):
+    return W.to_torch(a)
+
+
 # ----------------------------------------------------------------------------
-# workloads: inputs, algorithmic bytes / flops, and the call
+# workloads: inputs, algorithmic bytes / flops, the call, the oracle sample
 # ----------------------------------------------------------------------------
-def window_case(name):
-    if name == "vision_window_16384tok":
-        return W.vision_window(16384, W.SINK_KEY0_BIAS)
-    if name == "vision_window_4096tok":
-        return W.vision_window(4096, W.SINK_KEY0_BIAS)
-    if name == "gqa_window_16384tok":
-        return W.gqa_window(W.SINK_KEY0_BIAS)
-    raise SystemExit("unknown workload %s" % name)
-
-
-WORKLOADS = ["vision_window_16384tok", "vision_window_4096tok",
-             "gqa_window_16384tok"]
-
-
-def window_counts(c):
-    """Algorithmic bytes (q, o once; k, v once per KV head; LSE) and flops
-    (4 * D per live (row, key, head) triple) of one window call."""
-    T, hq, d = c.q.shape
-    hkv = c.k.shape[1]
-    nbytes = 2 * T * hq * d * 2 + 2 * T * hkv * d * 2 + hq * T * 4
-    cu = c.cu_seqlens.astype(np.int64)
-    live = 0
-    for b in range(len(cu) - 1):
-        n = int(cu[b + 1] - cu[b])
-        i = np.arange(n)
-        lo = np.maximum(0, i - c.window_left)
-        hi = np.minimum(n - 1, i + c.window_right)
-        live += int((hi - lo + 1).sum())
-    flops = 4 * d * live * hq
-    return nbytes, flops
-
-
-def window_config(c, name):
-    T, hq, d = c.q.shape
-    return {"workload": name, "tokens": int(T), "seqs": int(len(c.cu_seqlens) - 1),
-            "q_heads": int(hq), "kv_heads": int(c.k.shape[1]), "head_dim": int(d),
-            "window": int(c.window_left), "sink_mode": MODE_NAMES[c.mode]}
-
-
 class WindowRunner:
-    kernel_prefix = "window_fwd_kernel"
+    """sa_varlen_window_fwd on a packed window workload."""
+    bound = "hbm"
+    source = "attention_head_sinks_gb300/csrc/window_fwd.cu"
 
-    def __init__(self, c, nsets):
+    def __init__(self, name):
+        self.name = name
+        if name == "vision_window_16384tok":
+            self.c = W.vision_window(16384, W.SINK_KEY0_BIAS)
+        elif name == "vision_window_4096tok":
+            self.c = W.vision_window(4096, W.SINK_KEY0_BIAS)
+        else:
+            self.c = W.gqa_window(W.SINK_KEY0_BIAS)
+        self.mode = self.c.mode
+
+    def counts(self):
+        """Bytes: q, o once; k, v once per KV head; LSE.  Flops: 4 * D per live
+        (row, key, head)."""
+        c = self.c
+        T, hq, d = c.q.shape
+        hkv = c.k.shape[1]
+        nbytes = 2 * T * hq * d * 2 + 2 * T * hkv * d * 2 + hq * T * 4
+        cu = c.cu_seqlens.astype(np.int64)
+        live = 0
+        for b in range(len(cu) - 1):
+            n = int(cu[b + 1] - cu[b])
+            i = np.arange(n)
+            live += int((np.minimum(n - 1, i + c.window_right)
+                         - np.maximum(0, i - c.window_left) + 1).sum())
+        return nbytes, 4 * d * live * hq
+
+    def config(self):
+        c = self.c
+        T, hq, d = c.q.shape
+        return {"workload": self.name, "tokens": int(T),
+                "seqs": int(len(c.cu_seqlens) - 1), "q_heads": int(hq),
+                "kv_heads": int(c.k.shape[1]), "head_dim": int(d),
+                "window": int(c.window_left), "sink_mode": MODE_NAMES[self.mode]}
+
+    def setup(self, nsets):
         import torch
-        self.c = c
-        self.torch = torch
+        c = self.c
         dev = torch.device("cuda")
         self.sets = []
         for _ in range(nsets):
-            q, k, v = (W.to_torch(x).to(dev) for x in (c.q, c.k, c.v))
+            q, k, v = (_torch_bits(x).to(dev) for x in (c.q, c.k, c.v))
             out = torch.empty_like(q)
             lse = torch.empty((c.q.shape[1], c.q.shape[0]), dtype=torch.float32,
                               device=dev)
             self.sets.append((q, k, v, out, lse))
         self.cu = torch.from_numpy(c.cu_seqlens).to(dev)
         self.sinks = torch.from_numpy(c.sinks).to(dev)
-        self.set_bytes = sum(t.numel() * t.element_size() for t in self.sets[0])
+
+    def touched_bytes(self):
+        return self.counts()[0]
+
+    def launches_per_call(self):
+        return 1
 
     def call(self, i, mode=None):
         import attention_head_sinks_gb300 as sa
         q, k, v, out, lse = self.sets[i % len(self.sets)]
         c = self.c
         sa.sa_varlen_window_fwd(q, k, v, self.cu, c.window_left, c.window_right,
-                                self.sinks, c.mode if mode is None else mode,
+                                self.sinks, self.mode if mode is None else mode,
                                 c.scale, out=out, lse=lse)
 
-    def e2e(self, steps):
-        """Per step: pinned host inputs -> device, the call, out + LSE -> pinned
-        host.  Returns (us per step, h2d bytes, d2h bytes)."""
-        import attention_head_sinks_gb300 as sa
-        torch = self.torch
+    def host_io(self):
+        import torch
         c = self.c
-        host_in = [W.to_torch(x).pin_memory() for x in (c.q, c.k, c.v)] + \
-            [torch.from_numpy(c.cu_seqlens).pin_memory(),
-             torch.from_numpy(c.sinks).pin_memory()]
-        dev_in = [torch.empty_like(h, device="cuda") for h in host_in]
-        q, k, v, out, lse = self.sets[0]
-        host_out = [torch.empty_like(out, device="cpu").pin_memory(),
-                    torch.empty_like(lse, device="cpu").pin_memory()]
-        h2d = sum(h.numel() * h.element_size() for h in host_in)
-        d2h = sum(h.numel() * h.element_size() for h in host_out)
+        host_in = [_torch_bits(x) for x in (c.q, c.k, c.v)] + \
+            [torch.from_numpy(c.cu_seqlens), torch.from_numpy(c.sinks)]
+        out, lse = self.sets[0][3], self.sets[0][4]
 
-        def step():
-            for d_, h_ in zip(dev_in, host_in):
-                d_.copy_(h_, non_blocking=True)
+        def run(dev_in):
+            import attention_head_sinks_gb300 as sa
             sa.sa_varlen_window_fwd(dev_in[0], dev_in[1], dev_in[2], dev_in[3],
                                     c.window_left, c.window_right, dev_in[4],
-                                    c.mode, c.scale, out=out, lse=lse)
-            host_out[0].copy_(out, non_blocking=True)
-            host_out[1].copy_(lse, non_blocking=True)
+                                    self.mode, c.scale, out=out, lse=lse)
+        return host_in, [out, lse], run
 
-        for _ in range(3):
-            step()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(steps):
-            step()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) * 1000.0 / steps, h2d, d2h
+    def oracle_rows(self):
+        return self.c.q.shape[0]
+
+    def oracle(self, rows):
+        from oracle import sa_oracle
+        c = self.c
+        sa_oracle.window_fwd(c.q, c.k, c.v, c.cu_seqlens, c.window_left,
+                             c.window_right, c.sinks, self.mode, c.scale, rows=rows)
+
+
+class IndexRunner:
+    """sa_sparse_index_fwd on the sparse MLA decode workload."""
+    bound = "hbm"
+    source = "attention_head_sinks_gb300/csrc/sparse_index_fwd.cu"
+
+    def __init__(self, name):
+        self.name = name
+        self.c = W.mla_sparse_decode(W.SINK_NULL_LOGIT)
+        self.mode = self.c.mode
+
+    def counts(self):
+        """Bytes: q and o once, each listed (valid) latent row once per query,
+        the index list and the LSE.  Flops: (2 dqk + 2 dv) per (query, head,
+        valid key)."""
+        c = self.c
+        nq, hq, dqk = c.q.shape
+        valid = int(((c.indices >= 0) & (c.indices < c.num_kv)).sum())
+        nbytes = (nq * hq * dqk * 2 + nq * hq * c.dv * 2 + valid * dqk * 2
+                  + c.indices.nbytes + hq * nq * 4)
+        return nbytes, valid * hq * (2 * dqk + 2 * c.dv)
+
+    def config(self):
+        c = self.c
+        return {"workload": self.name, "queries": c.num_queries,
+                "q_heads": c.num_q_heads, "dqk": c.dqk, "dv": c.dv,
+                "kv_rows": c.num_kv, "topk": c.topk,
+                "valid_per_query": list(W.MLA_VALID_COUNTS),
+                "sink_mode": MODE_NAMES[self.mode]}
+
+    def setup(self, nsets):
+        import torch
+        import attention_head_sinks_gb300 as sa
+        c = self.c
+        dev = torch.device("cuda")
+        self.sets = []
+        for _ in range(nsets):
+            q, kv = _torch_bits(c.q).to(dev), _torch_bits(c.kv).to(dev)
+            idx = torch.from_numpy(c.indices).to(dev)
+            out = torch.empty((c.num_queries, c.num_q_heads, c.dv),
+                              dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((c.num_q_heads, c.num_queries), dtype=torch.float32,
+                              device=dev)
+            self.sets.append((q, kv, idx, out, lse))
+        self.sinks = torch.from_numpy(c.sinks).to(dev)
+        self.ws = torch.empty(max(1, sa.sa_sparse_index_workspace_size(
+            c.num_queries, c.num_q_heads, c.dv, c.topk)), dtype=torch.uint8, device=dev)
+
+    def touched_bytes(self):
+        return self.counts()[0]
+
+    def launches_per_call(self):
+        return 2 if self.c.topk > 256 else 1
+
+    def call(self, i, mode=None):
+        import attention_head_sinks_gb300 as sa
+        q, kv, idx, out, lse = self.sets[i % len(self.sets)]
+        c = self.c
+        sa.sa_sparse_index_fwd(q, kv, idx, c.dv, self.sinks,
+                               self.mode if mode is None else mode, c.scale,
+                               out=out, lse=lse, workspace=self.ws)
+
+    def host_io(self):
+        import torch
+        c = self.c
+        host_in = [_torch_bits(c.q), _torch_bits(c.kv), torch.from_numpy(c.indices),
+                   torch.from_numpy(c.sinks)]
+        out, lse = self.sets[0][3], self.sets[0][4]
+
+        def run(dev_in):
+            import attention_head_sinks_gb300 as sa
+            sa.sa_sparse_index_fwd(dev_in[0], dev_in[1], dev_in[2], c.dv, dev_in[3],
+                                   self.mode, c.scale, out=out, lse=lse,
+                                   workspace=self.ws)
+        return host_in, [out, lse], run
+
+    def oracle_rows(self):
+        return self.c.num_queries
+
+    def oracle(self, rows):
+        from oracle import sa_oracle
+        c = self.c
+        sa_oracle.sparse_index_fwd(c.q, c.kv, c.indices, c.dv, c.sinks, self.mode,
+                                   c.scale, rows=rows)
+
+
+class BlockRunner:
+    """sa_block_sparse_fwd on the DSA-style block-sparse prefill."""
+    bound = "tensor"
+    source = "attention_head_sinks_gb300/csrc/block_sparse_fwd.cu"
+
+    def __init__(self, name):
+        self.name = name
+        self.c = W.dsa_block_prefill(W.SINK_NULL_LOGIT)
+        self.mode = self.c.mode
+
+    def counts(self):
+        """Bytes: q, o once; k, v once per KV head; table; LSE.  Flops counted
+        over the selected blocks: 4 * D * 64 per (token, head, selected
+        block)."""
+        c = self.c
+        T, hq, d = c.q.shape
+        hkv = c.k.shape[1]
+        nbytes = 2 * T * hq * d * 2 + 2 * T * hkv * d * 2 + c.block_table.nbytes + hq * T * 4
+        nsel = int(((c.block_table >= 0) & (c.block_table < c.seq_len // c.block_size)).sum())
+        return nbytes, nsel * c.block_size * hq * 4 * d
+
+    def config(self):
+        c = self.c
+        return {"workload": self.name, "batch": c.batch, "seq_len": c.seq_len,
+                "q_heads": c.num_q_heads, "kv_heads": c.num_kv_heads,
+                "head_dim": c.head_dim, "block_size": c.block_size,
+                "topk_blocks": c.topk_blocks, "docs_per_row": 3,
+                "sink_mode": MODE_NAMES[self.mode],
+                "flops_basis": "selected blocks"}
+
+    def setup(self, nsets):
+        import torch
+        c = self.c
+        dev = torch.device("cuda")
+        self.sets = []
+        for _ in range(nsets):
+            q, k, v = (_torch_bits(x).to(dev) for x in (c.q, c.k, c.v))
+            out = torch.empty_like(q)
+            lse = torch.empty((c.num_q_heads, c.total_tokens), dtype=torch.float32,
+                              device=dev)
+            self.sets.append((q, k, v, out, lse))
+        self.table = torch.from_numpy(c.block_table).to(dev)
+        self.cu = torch.from_numpy(c.cu_docs).to(dev)
+        self.sinks = torch.from_numpy(c.sinks).to(dev)
+
+    def touched_bytes(self):
+        return self.counts()[0]
+
+    def launches_per_call(self):
+        return 1
+
+    def call(self, i, mode=None):
+        import attention_head_sinks_gb300 as sa
+        q, k, v, out, lse = self.sets[i % len(self.sets)]
+        c = self.c
+        sa.sa_block_sparse_fwd(q, k, v, c.batch, c.seq_len, self.table, c.block_size,
+                               self.cu, self.sinks, self.mode if mode is None else mode,
+                               c.scale, out=out, lse=lse)
+
+    def host_io(self):
+        import torch
+        c = self.c
+        host_in = [_torch_bits(x) for x in (c.q, c.k, c.v)] + \
+            [torch.from_numpy(c.block_table), torch.from_numpy(c.cu_docs),
+             torch.from_numpy(c.sinks)]
+        out, lse = self.sets[0][3], self.sets[0][4]
+
+        def run(dev_in):
+            import attention_head_sinks_gb300 as sa
+            sa.sa_block_sparse_fwd(dev_in[0], dev_in[1], dev_in[2], c.batch, c.seq_len,
+                                   dev_in[3], c.block_size, dev_in[4], dev_in[5],
+                                   self.mode, c.scale, out=out, lse=lse)
+        return host_in, [out, lse], run
+
+    def oracle_rows(self):
+        return self.c.total_tokens
+
+    def oracle(self, rows):
+        from oracle import sa_oracle
+        c = self.c
+        sa_oracle.block_sparse_fwd(c.q, c.k, c.v, c.batch, c.seq_len, c.block_table,
+                                   c.block_size, c.cu_docs, c.sinks, self.mode,
+                                   c.scale, rows=rows)
+
+
+RUNNERS = {
+    "vision_window_16384tok": WindowRunner,
+    "vision_window_4096tok": WindowRunner,
+    "gqa_window_16384tok": WindowRunner,
+    "mla_sparse_decode": IndexRunner,
+    "dsa_block_prefill": BlockRunner,
+}
 
 
 # ----------------------------------------------------------------------------
@@ -225,8 +403,9 @@ def kernel_source_hash(path):
 
 
 def recorded_traffic(workload, src_hash):
-    """DRAM bytes per launch from an ncu capture summarised in
-    profiles/dram_traffic.txt, valid only for the same kernel source."""
+    """DRAM bytes per launch of the dominant kernel from an ncu capture
+    summarised in profiles/dram_traffic.txt, valid only for the same kernel
+    source."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -241,81 +420,90 @@ def recorded_traffic(workload, src_hash):
 # ----------------------------------------------------------------------------
 # CPU oracle (baseline and reference arm)
 # ----------------------------------------------------------------------------
-def oracle_window_sample(c, rows):
-    from oracle import sa_oracle
+def _oracle_time(runner, rows):
     t0 = time.perf_counter()
-    sa_oracle.window_fwd(c.q, c.k, c.v, c.cu_seqlens, c.window_left,
-                         c.window_right, c.sinks, c.mode, c.scale, rows=rows)
+    runner.oracle(rows)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(c, budget_s=10.0):
+def sample_spans(total, nrows, nspans=8):
+    """``nspans`` equal spans spread evenly over [0, total), ``nrows`` rows in
+    all (so the sample sees every part of the workload)."""
+    per = max(1, nrows // nspans)
+    step = max(per, total // nspans)
+    return [(s, min(total, s + per)) for s in range(0, total, step)][:nspans]
+
+
+def cpu_baseline(runner, budget_s=10.0):
     from oracle import sa_oracle
-    T = c.q.shape[0]
-    rows = min(T, 512)
-    dt = oracle_window_sample(c, (0, rows))
-    # grow the sample to ~budget_s of CPU work, bounded by the whole call
-    want = int(rows * budget_s / max(dt, 1e-6))
-    rows2 = int(min(T, max(rows, want)))
-    dt2 = oracle_window_sample(c, (0, rows2))
-    us = dt2 * 1e6 * T / rows2
+    total = runner.oracle_rows()
+    probe = sample_spans(total, max(8, total // 64))
+    dt = sum(_oracle_time(runner, r) for r in probe)
+    nprobe = sum(e - s for s, e in probe)
+    want = int(nprobe * budget_s / max(dt, 1e-6))
+    nrows = int(min(total, max(nprobe, want)))
+    spans = sample_spans(total, nrows)
+    dt = sum(_oracle_time(runner, r) for r in spans)
+    n = sum(e - s for s, e in spans)
+    us = dt * 1e6 * total / n
     return {"value": round(us, 1), "unit": "us/call", "cores": sa_oracle.num_threads(),
             "kind": "oracle",
-            "sample": "%d of %d query tokens (all heads), fp64 C oracle with OpenMP; "
-                      "scaled to one call" % (rows2, T)}
+            "sample": "%d of %d query rows in %d evenly spread spans (all heads), fp64 C "
+                      "oracle with OpenMP; scaled to one call" % (n, total, len(spans))}
 
 
-def run_reference(args, rank, world):
+def run_reference(args, rank):
     if rank != 0:
         return
     from oracle import sa_oracle
-    c = window_case(args.workload)
-    T = c.q.shape[0]
-    rows = max(1, T // 128)            # each step: 1/128 of the call
-    starts = [(i * rows) % T for i in range(args.steps + args.warmup)]
+    runner = RUNNERS[args.workload](args.workload)
+    total = runner.oracle_rows()
+    per = max(1, total // 128)           # each step: 1/128 of the call's rows
+    nspan = max(1, total // per)
+    starts = [((i % nspan) * per) for i in range(args.steps + args.warmup)]
     for s in starts[:args.warmup]:
-        oracle_window_sample(c, (s, min(T, s + rows)))
+        _oracle_time(runner, (s, min(total, s + per)))
     t0 = time.perf_counter()
     for s in starts[args.warmup:]:
-        oracle_window_sample(c, (s, min(T, s + rows)))
+        _oracle_time(runner, (s, min(total, s + per)))
     dt = time.perf_counter() - t0
-    us_call = dt * 1e6 / max(args.steps, 1) * (T / rows)
+    us_call = dt * 1e6 / max(args.steps, 1) * (total / per)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(us_call, 1),
         "unit": "us/call", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / max(args.steps, 1), 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic", "config": window_config(c, args.workload),
+        "dtype": "f64", "data": "synthetic", "config": runner.config(),
         "cpu_baseline": {"value": round(us_call, 1), "unit": "us/call",
                          "cores": sa_oracle.num_threads(), "kind": "oracle",
-                         "sample": "each step %d of %d query tokens (all heads); "
-                                   "value scaled to one call" % (rows, T)},
+                         "sample": "each step %d of %d query rows (all heads), walking "
+                                   "the call in order; value scaled to one call"
+                                   % (per, total)},
         "e2e": {"value": round(us_call, 1), "unit": "us/call",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-METRIC = "attn fwd us/call (achieved HBM GB/s as % of GB300 roofline)"
-
-
 # ----------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="vision_window_16384tok", choices=WORKLOADS)
+    ap.add_argument("--workload", default="vision_window_16384tok", choices=sorted(RUNNERS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--e2e-steps", type=int, default=50)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.steps is None:
+        args.steps = 500 if args.workload == "dsa_block_prefill" else 5000
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        run_reference(args, rank)
         return
 
     import torch
@@ -331,18 +519,16 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    c = window_case(args.workload)
-    nbytes, flops = window_counts(c)
-    runner = WindowRunner(c, nsets=1)
-    nsets = max(2, -(-3 * L2_BYTES // runner.set_bytes))
-    runner = WindowRunner(c, nsets=nsets)
+    runner = RUNNERS[args.workload](args.workload)
+    nbytes, flops = runner.counts()
+    nsets = max(2, -(-3 * L2_BYTES // runner.touched_bytes()))
+    runner.setup(nsets)
 
     for i in range(args.warmup):
         runner.call(i)
     barrier()
 
-    # sink cost: the same kernel with sinks disabled, timed the same way
-    def timed(mode, steps, sampler=None):
+    def timed(mode, steps):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -354,14 +540,13 @@ def main():
             ends[i].record()
         e1.record()
         barrier()
-        total_ms = e0.elapsed_time(e1)
         per = [s.elapsed_time(e) * 1000.0 for s, e in zip(starts, ends)]
-        return total_ms, per
+        return e0.elapsed_time(e1), per
 
     sampler = ClockSampler(gpu_uuid())
-    total_ms, per = timed(c.mode, args.steps)
+    total_ms, per = timed(runner.mode, args.steps)
     clocks = sampler.stop()
-    total_none, per_none = timed(W.SINK_NONE, max(args.steps // 4, 10))
+    _, per_none = timed(W.SINK_NONE, max(args.steps // 4, 10))
 
     step_ms = total_ms / args.steps
     if dist is not None:
@@ -371,8 +556,32 @@ def main():
     kern_us = statistics.mean(per)
     kern_us_none = statistics.mean(per_none)
 
-    e2e_us, h2d, d2h = runner.e2e(args.e2e_steps)
-    err = None
+    # end to end: pinned host inputs -> device, the call, results -> host
+    host_in, dev_out, run = runner.host_io()
+    host_in = [h.pin_memory() for h in host_in]
+    dev_in = [torch.empty_like(h, device="cuda") for h in host_in]
+    host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in dev_out]
+
+    def e2e_step():
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        run(dev_in)
+        for h_, o_ in zip(host_out, dev_out):
+            h_.copy_(o_, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_us = e0.elapsed_time(e1) * 1000.0 / args.e2e_steps
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = sum(h.numel() * h.element_size() for h in host_out)
+
     import attention_head_sinks_gb300 as sa
     err = sa.sa_device_error()
 
@@ -382,13 +591,25 @@ def main():
         return
 
     hbm_peak, tf_peak, peak_src = measured_peaks()
-    achieved = nbytes / (kern_us * 1e-6) / 1e9
-    src_hash = kernel_source_hash("attention_head_sinks_gb300/csrc/window_fwd.cu")
+    src_hash = kernel_source_hash(runner.source)
+    traffic = recorded_traffic(args.workload, src_hash)
+    gbs = nbytes / (kern_us * 1e-6) / 1e9
+    tfs = flops / (kern_us * 1e-6) / 1e12
+    if runner.bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": traffic}
+        other = {"alg_tflops": round(tfs, 2), "frac_of_bf16_peak": round(tfs / tf_peak, 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tfs, 1), "peak": tf_peak,
+                "unit": "TFLOP/s", "frac": round(tfs / tf_peak, 4), "traffic": traffic}
+        other = {"alg_gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm_peak, 4)}
+    roof.update({"peak_source": peak_src, "alg_bytes": nbytes, "alg_flops": flops,
+                 "kernel_us": round(kern_us, 3), "source_hash": src_hash})
     value_us = step_ms * 1000.0 / world
-    cfg = window_config(c, args.workload)
+    cfg = runner.config()
     cfg.update({"global_batch": world, "parallelism": "replicas x%d" % world,
-                "l2": "%d rotating input sets (%.0f MB) > 129 MB L2" %
-                      (nsets, nsets * runner.set_bytes / 1e6)})
+                "l2": "%d rotating input sets (%.0f MB touched) > 129 MB L2" %
+                      (nsets, nsets * runner.touched_bytes() / 1e6)})
     line = {
         "metric": METRIC,
         "value": round(value_us, 3),
@@ -404,24 +625,18 @@ def main():
         "dtype": "bf16",
         "data": "synthetic",
         "config": cfg,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4),
-                     "traffic": recorded_traffic(args.workload, src_hash),
-                     "peak_source": peak_src, "alg_bytes": nbytes,
-                     "kernel_us": round(kern_us, 3)},
-        "tensor": {"alg_tflops": round(flops / (kern_us * 1e-6) / 1e12, 2),
-                   "frac_of_peak": round(flops / (kern_us * 1e-6) / 1e12 / tf_peak, 4)},
+        "roofline": roof,
+        "secondary": other,
         "sink_cost": round(kern_us / kern_us_none - 1.0, 4),
         "kernel_us_sinks_disabled": round(kern_us_none, 3),
         "e2e": {"value": round(e2e_us, 2), "unit": "us/call",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * runner.launches_per_call(),
         "clocks": clocks,
         "device_error": err,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(c)
+        line["cpu_baseline"] = cpu_baseline(runner)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
