@@ -10,19 +10,21 @@
 // Layout: the latent row holds 576 values (512 latent + 64 rope); K is the
 // whole row and V its first 512 values, shared by all query heads.
 //
-// Work split.  The index list of a query is cut into slices of 256 slots and
-// V's 512 columns into two halves.  One CTA takes (slice, half, query, block of
-// up to 128 heads):
+// Work split.  The index list of a query is cut into slices of 256 slots; one
+// CTA takes (query, slice, block of up to 128 heads):
 //   S = Q K^T        M = 128 heads, N = valid keys of the slice (rounded to 16),
 //                    K = 576 in nine 64-wide slabs;
-//   O_half = P V     N = 256 V columns, K = the slice's keys.
+//   O_half = P V     twice, N = 256 V columns each, K = the slice's keys.
 // Tensor memory: S at columns [0, 256) (P in place, bf16, the A operand of the
-// PV MMA), O_half at [256, 512).  Shared memory: the four 64-column slabs of
-// the gathered rows that form this CTA's V half stay resident (they are also
-// four of the nine K slabs); the other five K slabs and the nine Q slabs
-// stream through a two-stage ring.  Rows are gathered by TMA tile::gather4
-// into 128-byte-swizzled slabs, which are both the K-major B operand of S and
-// the MN-major B operand of O.
+// PV MMAs), O_half at [256, 512), reused by the second half.  Shared memory:
+// slabs 0..3 of the gathered rows (V columns 0..255, also K slabs) stay
+// resident; K slabs 4..8 and the nine Q slabs stream through two-stage rings;
+// after the first P V, slabs 4..7 are gathered again (from L2) over the
+// resident buffer for the second.  Warps 0..3 own the 128 head rows (softmax,
+// epilogue; thread 0 issues the MMAs, thread 32 loads Q by TMA); warps 4..7
+// gather the key rows with 16-byte cp.async copies straight into
+// 128-byte-swizzled slabs -- the K-major B operand of S and the MN-major B
+// operand of O.
 // A query whose valid keys all sit in one slice is finished by that CTA
 // (sink fold, bf16 O, LSE); otherwise each slice writes (O, m, l) partials
 // and the combine kernel merges them and folds the sink once.
@@ -70,45 +72,60 @@ struct IndexParams {
 };
 
 struct __align__(8) IndexSmemCtl {
-  uint64_t res_full[kHalfSlabs];
-  uint64_t step_full[kStages];
-  uint64_t step_empty[kStages];
+  uint64_t res_full;         // resident slabs 0..3 gathered
+  uint64_t res2_full;        // slabs 4..7 gathered over them for the second V half
+  uint64_t kst_full[kStages];
+  uint64_t kst_empty[kStages];
+  uint64_t q_full[kStages];
+  uint64_t q_empty[kStages];
   uint64_t s_full;
-  uint64_t o_full;
+  uint64_t o_full;           // phase 0: first V half, phase 1: second
   uint32_t tmem_base;
-  int32_t n_slice;
-  int32_t nonempty;
   int32_t warp_cnt[4][kMaxSlices];
   int32_t warp_ofs[2][4];
   int32_t kidx[kSliceKeys];
 };
 
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map,
-                                            uint64_t* bar, int x, int r0, int r1,
-                                            int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::"
-      "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-      : "memory");
+// K slab used at S step j: slabs 4..8 stream through the ring first, then
+// the resident slabs 0..3 (which are also V columns 0..255).
+__device__ __forceinline__ int step_slab(int j) { return j < 5 ? 4 + j : j - 5; }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void bar_rows() {  // the four row warps only
+  asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
-// K slab id used at pipeline step j for V half `half`: the five slabs outside
-// the half first (streamed), then the half's four (resident).
-__device__ __forceinline__ int step_slab(int j, int half) {
-  if (j < 5) {
-    // streamed: half 0 -> 4,5,6,7,8 ; half 1 -> 0,1,2,3,8
-    if (j == 4) return 8;
-    return half == 0 ? 4 + j : j;
+// Gather 64 columns (slab `slab`) of the slice's npad key rows into a
+// 128-byte-swizzled [npad][64] bf16 slab at dst; rows past n are zero.
+// Thread gt of 128 copies 16-byte chunks gt, gt + 128, ... (8 per row).
+__device__ __forceinline__ void gather_slab(uint32_t dst, const uint16_t* kv,
+                                            const int32_t* kidx, int n, int npad, int slab,
+                                            int gt) {
+  for (int ch = gt; ch < npad * 8; ch += 128) {
+    const int r = ch >> 3, c = ch & 7;
+    const bool live = r < n;
+    const uint16_t* src = kv + (live ? (int64_t)kidx[r] * kDqk + slab * kSlab + c * 8 : 0);
+    cp_async16(dst + r * 128 + ((c ^ (r & 7)) << 4), src, live ? 16u : 0u);
   }
-  return half * kHalfSlabs + (j - 5);
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(128, 1)
-sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
-                        const __grid_constant__ CUtensorMap tm_kv,
+__global__ void __launch_bounds__(256, 1)
+sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const uint16_t* kv,
                         const IndexParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ IndexSmemCtl ctl;
@@ -118,56 +135,45 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint8_t* s_kst = s_res + kHalfSlabs * kSlabBytesK;       // 2 x 32 KB
   uint8_t* s_qst = s_kst + kStages * kSlabBytesK;          // 2 x 16 KB
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   const int q = blockIdx.x;
-  const int half = blockIdx.y & 1;
-  const int hb = blockIdx.y >> 1;
+  const int hb = blockIdx.y;
   const int slice = blockIdx.z;
   const int32_t* idx_row = p.indices + (int64_t)q * p.topk;
 
-  // ---- count valid entries per slice; compact this slice's indices --------
-  for (int s = threadIdx.x; s < 4 * kMaxSlices; s += 128)
-    (&ctl.warp_cnt[0][0])[s] = 0;
-  __syncthreads();
-  for (int k = 0; k * 128 < p.topk; k += 2) {
-    // entries 128k + t and 128(k+1) + t both fall in slice k / 2
-    int c = 0;
+  // ---- compact this slice's valid indices (warps 0..3) ---------------------
+  int32_t my_idx[2] = {-1, -1};
+  bool my_ok[2] = {false, false};
+  if (tid < 128) {
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const int e = (k + u) * 128 + threadIdx.x;
-      if (e < p.topk) {
-        const int32_t j = __ldg(idx_row + e);
-        c += (j >= 0 && (int64_t)j < p.num_kv) ? 1 : 0;
+      const int e = slice * kSliceKeys + u * 128 + tid;
+      my_idx[u] = (e < p.topk) ? __ldg(idx_row + e) : -1;
+      my_ok[u] = my_idx[u] >= 0 && (int64_t)my_idx[u] < p.num_kv;
+      const uint32_t bal = __ballot_sync(0xffffffffu, my_ok[u]);
+      if (lane == 0) ctl.warp_ofs[u][warp] = __popc(bal);
+    }
+  }
+  __syncthreads();
+  int n = 0;
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+    n += ctl.warp_ofs[u][0] + ctl.warp_ofs[u][1] + ctl.warp_ofs[u][2] + ctl.warp_ofs[u][3];
+  if (n == 0 && slice != 0) {
+    // Empty slice: record (m, l) = (-inf, 0) so that a reused workspace never
+    // holds stale entries for the combine to read, and leave.
+    if (tid < 128 && p.part_ml) {
+      const int h = hb * 128 + tid;
+      if (h < p.num_q_heads) {
+        float* ml = p.part_ml + (((int64_t)q * p.nslices + slice) * p.num_q_heads + h) * 2;
+        ml[0] = -INFINITY;
+        ml[1] = 0.f;
       }
     }
-    c = __reduce_add_sync(0xffffffffu, c);
-    if (lane == 0) ctl.warp_cnt[warp][k >> 1] = c;
+    return;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int nonempty = 0, mine = 0;
-    for (int s = 0; s < p.nslices; ++s) {
-      const int c = ctl.warp_cnt[0][s] + ctl.warp_cnt[1][s] + ctl.warp_cnt[2][s] +
-                    ctl.warp_cnt[3][s];
-      nonempty += c > 0 ? 1 : 0;
-      if (s == slice) mine = c;
-    }
-    ctl.nonempty = nonempty;
-    ctl.n_slice = mine;
-  }
-  // compaction of slice entries (order preserved)
-  int32_t my_idx[2];
-  bool my_ok[2];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int e = slice * kSliceKeys + u * 128 + threadIdx.x;
-    my_idx[u] = (e < p.topk) ? __ldg(idx_row + e) : -1;
-    my_ok[u] = my_idx[u] >= 0 && (int64_t)my_idx[u] < p.num_kv;
-    const uint32_t bal = __ballot_sync(0xffffffffu, my_ok[u]);
-    if (lane == 0) ctl.warp_ofs[u][warp] = __popc(bal);
-  }
-  __syncthreads();
-  {
+  if (tid < 128) {
     int base = 0;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -178,40 +184,62 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       base += ctl.warp_ofs[u][0] + ctl.warp_ofs[u][1] + ctl.warp_ofs[u][2] +
               ctl.warp_ofs[u][3];
     }
+    // non-empty slices of the whole row (decides final output vs partial)
+    for (int s2 = tid; s2 < 4 * kMaxSlices; s2 += 128) (&ctl.warp_cnt[0][0])[s2] = 0;
   }
   __syncthreads();
-  const int n = ctl.n_slice;
-  const int nonempty = ctl.nonempty;
-  const int row = threadIdx.x;
-  const int h = hb * 128 + row;
-  const bool row_valid = h < p.num_q_heads;
-  const float sink2 = (MODE != SA_SINK_NONE && row_valid) ? __ldg(p.sinks + h) * kLog2e : 0.f;
+  if (tid < 128) {
+    for (int k = 0; k * 128 < p.topk; k += 2) {
+      // entries 128k + t and 128(k+1) + t both fall in slice k / 2
+      int c = 0;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int e = (k + u) * 128 + tid;
+        if (e < p.topk) {
+          const int32_t jj = __ldg(idx_row + e);
+          c += (jj >= 0 && (int64_t)jj < p.num_kv) ? 1 : 0;
+        }
+      }
+      c = __reduce_add_sync(0xffffffffu, c);
+      if (lane == 0) ctl.warp_cnt[warp][k >> 1] = c;
+    }
+  }
+  __syncthreads();
+  int nonempty = 0;
+  for (int s2 = 0; s2 < p.nslices; ++s2)
+    nonempty += (ctl.warp_cnt[0][s2] + ctl.warp_cnt[1][s2] + ctl.warp_cnt[2][s2] +
+                 ctl.warp_cnt[3][s2]) > 0 ? 1 : 0;
   const bool direct = nonempty <= 1;  // this CTA produces the final output
 
   if (n == 0) {
-    // every slice records its (m, l) so that a reused workspace never holds
-    // stale entries for the combine to read
-    if (p.part_ml && half == 0 && row_valid) {
-      float* ml = p.part_ml + (((int64_t)q * p.nslices + slice) * p.num_q_heads + h) * 2;
-      ml[0] = -INFINITY;
-      ml[1] = 0.f;
-    }
-    if (nonempty == 0 && slice == 0 && row_valid) {
-      // empty key set: zero output, LSE = -inf
-      uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)q * p.num_q_heads + h) * kDv +
-                                            half * 256);
-      for (int i = 0; i < 32; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-      if (half == 0) p.lse[(int64_t)h * p.nq + q] = -INFINITY;
+    // slice 0 of a row: an empty key set gets zero output and LSE = -inf
+    if (tid < 128) {
+      const int h = hb * 128 + tid;
+      if (h < p.num_q_heads) {
+        if (p.part_ml) {
+          float* ml = p.part_ml + (((int64_t)q * p.nslices + slice) * p.num_q_heads + h) * 2;
+          ml[0] = -INFINITY;
+          ml[1] = 0.f;
+        }
+        if (nonempty == 0) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)q * p.num_q_heads + h) * kDv);
+          for (int i = 0; i < kDv / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+          p.lse[(int64_t)h * p.nq + q] = -INFINITY;
+        }
+      }
     }
     return;
   }
   const int npad = (n + 15) & ~15;  // MMA N and gathered rows
 
-  if (threadIdx.x == 0) {
-    for (int r = 0; r < kHalfSlabs; ++r) mbar_init(&ctl.res_full[r], 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ctl.step_full[s], 1);
-      mbar_init(&ctl.step_empty[s], 1);
+  if (tid == 0) {
+    mbar_init(&ctl.res_full, 128);
+    mbar_init(&ctl.res2_full, 128);
+    for (int s2 = 0; s2 < kStages; ++s2) {
+      mbar_init(&ctl.kst_full[s2], 128);
+      mbar_init(&ctl.kst_empty[s2], 1);
+      mbar_init(&ctl.q_full[s2], 1);
+      mbar_init(&ctl.q_empty[s2], 1);
     }
     mbar_init(&ctl.s_full, 1);
     mbar_init(&ctl.o_full, 1);
@@ -226,221 +254,282 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   const int qrow0 = q * p.num_q_heads + hb * 128;  // first Q row of this block
-  bool ok = true;
 
-  if (threadIdx.x == 32) {
-    // ---- producer ---------------------------------------------------------
-    tma_prefetch_map(&tm_q);
-    tma_prefetch_map(&tm_kv);
-    const uint32_t slab_bytes = (uint32_t)npad * 128u;
-    for (int r = 0; r < kHalfSlabs; ++r) {
-      const int slab = half * kHalfSlabs + r;
-      mbar_arrive_expect_tx(&ctl.res_full[r], slab_bytes);
-      for (int g = 0; g < npad; g += 4) {
-        const int r0 = g + 0 < n ? ctl.kidx[g + 0] : -1;
-        const int r1 = g + 1 < n ? ctl.kidx[g + 1] : -1;
-        const int r2 = g + 2 < n ? ctl.kidx[g + 2] : -1;
-        const int r3 = g + 3 < n ? ctl.kidx[g + 3] : -1;
-        tma_gather4(s_res + r * kSlabBytesK + g * 128, &tm_kv, &ctl.res_full[r],
-                    slab * kSlab, r0, r1, r2, r3);
-      }
-    }
-    for (int j = 0; j < kNumQkSlabs && ok; ++j) {
+  if (warp >= 4) {
+    // ---- gatherers (warps 4..7) --------------------------------------------
+    const int gt = tid - 128;
+    bool ok = true;
+    // resident slabs 0..3 first (one cp.async group)
+    for (int r = 0; r < kHalfSlabs; ++r)
+      gather_slab(smem_u32(s_res + r * kSlabBytesK), kv, ctl.kidx, n, npad, r, gt);
+    cp_async_commit();
+    // streamed slabs 4..8 through the two-stage ring
+    for (int j = 0; j < 5; ++j) {
       const int st = j & 1;
-      const int use = j >> 1;
-      if (j >= kStages) ok = mbar_wait(&ctl.step_empty[st], (use - 1) & 1, p.err, kErrWaitFree);
-      if (!ok) break;
-      const int slab = step_slab(j, half);
-      const bool streamed = j < 5;
-      mbar_arrive_expect_tx(&ctl.step_full[st],
-                            kSlabBytesQ + (streamed ? slab_bytes : 0u));
-      tma_load_2d(s_qst + st * kSlabBytesQ, &tm_q, &ctl.step_full[st], slab * kSlab, qrow0);
-      if (streamed) {
-        for (int g = 0; g < npad; g += 4) {
-          const int r0 = g + 0 < n ? ctl.kidx[g + 0] : -1;
-          const int r1 = g + 1 < n ? ctl.kidx[g + 1] : -1;
-          const int r2 = g + 2 < n ? ctl.kidx[g + 2] : -1;
-          const int r3 = g + 3 < n ? ctl.kidx[g + 3] : -1;
-          tma_gather4(s_kst + st * kSlabBytesK + g * 128, &tm_kv, &ctl.step_full[st],
-                      slab * kSlab, r0, r1, r2, r3);
+      if (j >= kStages && ok)
+        ok = mbar_wait(&ctl.kst_empty[st], ((j >> 1) - 1) & 1, p.err, kErrWaitFree);
+      if (ok) gather_slab(smem_u32(s_kst + st * kSlabBytesK), kv, ctl.kidx, n, npad, 4 + j, gt);
+      cp_async_commit();
+      // every group but the newest has landed: publish it
+      cp_async_wait<1>();
+      fence_proxy_async();
+      if (j == 0) mbar_arrive(&ctl.res_full);
+      else mbar_arrive(&ctl.kst_full[(j - 1) & 1]);
+    }
+    cp_async_wait<0>();
+    fence_proxy_async();
+    mbar_arrive(&ctl.kst_full[4 & 1]);
+    // second V half: once P V of the first half is done, slabs 4..7 replace
+    // slabs 0..3 in the resident buffer
+    if (ok) ok = mbar_wait(&ctl.o_full, 0, p.err, kErrWaitMma);
+    if (ok)
+      for (int r = 0; r < kHalfSlabs; ++r)
+        gather_slab(smem_u32(s_res + r * kSlabBytesK), kv, ctl.kidx, n, npad, 4 + r, gt);
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async();
+    mbar_arrive(&ctl.res2_full);
+  } else {
+    // ---- warps 0..3: MMA issue (thread 0), softmax and epilogue (rows) -----
+    const int row = tid;
+    const int h = hb * 128 + row;
+    const bool row_valid = h < p.num_q_heads;
+    const float sink2 = (MODE != SA_SINK_NONE && row_valid) ? __ldg(p.sinks + h) * kLog2e : 0.f;
+    bool ok = true;
+    if (tid == 0) {
+      const uint32_t idesc = idesc_bf16(128, npad, false);
+      for (int j = 0; j < kNumQkSlabs && ok; ++j) {
+        const int st = j & 1;
+        ok = mbar_wait(&ctl.q_full[st], (j >> 1) & 1, p.err, kErrWaitLoad);
+        if (ok && j < 5) ok = mbar_wait(&ctl.kst_full[st], (j >> 1) & 1, p.err, kErrWaitLoad);
+        if (ok && j == 5) ok = mbar_wait(&ctl.res_full, 0, p.err, kErrWaitLoad);
+        if (!ok) break;
+        tc_fence_after();
+        const uint8_t* kb = j < 5 ? s_kst + st * kSlabBytesK : s_res + (j - 5) * kSlabBytesK;
+        const uint8_t* qb = s_qst + st * kSlabBytesQ;
+#pragma unroll
+        for (int kk = 0; kk < kSlab / 16; ++kk) {
+          const uint64_t a = smem_desc(smem_u32(qb) + kk * 32, 16, 1024, kLayoutSw128);
+          const uint64_t b = smem_desc(smem_u32(kb) + kk * 32, 16, 1024, kLayoutSw128);
+          mma_ss(tmem + kColS, a, b, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&ctl.q_empty[st]);
+        if (j < 5) mma_commit(&ctl.kst_empty[st]);
+      }
+      if (ok) mma_commit(&ctl.s_full);
+      else mbar_arrive(&ctl.s_full);
+    } else if (tid == 32) {
+      // Q slab of each S step by TMA through its two-stage ring
+      tma_prefetch_map(&tm_q);
+      int issued = 0;
+      for (int j = 0; j < kNumQkSlabs; ++j) {
+        const int st = j & 1;
+        if (j >= kStages && !mbar_wait(&ctl.q_empty[st], ((j >> 1) - 1) & 1, p.err, kErrWaitFree))
+          break;
+        mbar_arrive_expect_tx(&ctl.q_full[st], kSlabBytesQ);
+        tma_load_2d(s_qst + st * kSlabBytesQ, &tm_q, &ctl.q_full[st], step_slab(j) * kSlab,
+                    qrow0);
+        ++issued;
+      }
+      // bounded drain of the last copies (immediate once the MMAs consumed them)
+      for (int j = max(0, issued - kStages); j < issued; ++j)
+        mbar_wait(&ctl.q_full[j & 1], (j >> 1) & 1, p.err, kErrWaitDrain);
+    }
+
+    // ---- softmax over the slice's keys (thread = head row) -----------------
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    ok = mbar_wait(&ctl.s_full, 0, p.err, kErrWaitMma) && ok;
+    __syncwarp();
+    tc_fence_after();
+    const float c2 = p.scale_log2;
+    const int nch = (npad + 31) >> 5;
+    float mr[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mr[e] = -INFINITY;
+    for (int c = 0; c < nch; ++c) {
+      float sv[32];
+      tmem_ld32(lane_base + kColS + 32 * c, sv);
+      tmem_wait_ld();
+      const int c0 = 32 * c;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) mr[e & 7] = fmaxf(mr[e & 7], (c0 + e < n) ? sv[e] : -INFINITY);
+    }
+    // max(s) * c2 == max(s * c2) exactly (c2 > 0, rounding is monotone)
+    const float m = fmaxf(fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])),
+                          fmaxf(fmaxf(mr[4], mr[5]), fmaxf(mr[6], mr[7]))) * c2;
+    float lp[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) lp[e] = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      float sv[32];
+      tmem_ld32(lane_base + kColS + 32 * c, sv);
+      tmem_wait_ld();
+      const int c0 = 32 * c;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        sv[e] = (c0 + e < n) ? ex2_approx(fmaf(sv[e], c2, -m)) : 0.f;
+        lp[e & 7] += sv[e];
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(sv[2 * e], sv[2 * e + 1]);
+      tmem_st16(lane_base + kColS + 16 * c, pk);
+    }
+    const float l = ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
+    tmem_wait_st();
+    float inv;
+    {
+      float den = l, alpha = 1.f;
+      if (MODE == SA_SINK_NULL_LOGIT) {
+        const float mp = fmaxf(m, sink2);
+        alpha = ex2_approx(m - mp);
+        den = l * alpha + ex2_approx(sink2 - mp);
+      }
+      inv = alpha / den;
+    }
+
+    // ---- the two V halves: O_half = P V_half, then store -------------------
+    for (int half = 0; half < 2; ++half) {
+      tc_fence_before();
+      bar_rows();
+      if (tid == 0) {
+        tc_fence_after();
+        bool go = ok;
+        if (go && half == 1) go = mbar_wait(&ctl.res2_full, 0, p.err, kErrWaitLoad);
+        if (go) {
+          const uint32_t idesc = idesc_bf16(128, 256, true);
+          for (int kk = 0; kk < npad / 16; ++kk) {
+            const uint64_t b = smem_desc(smem_u32(s_res) + kk * 16 * 128, kSlabBytesK, 1024,
+                                         kLayoutSw128);
+            mma_ts(tmem + kColO, tmem + kColS + kk * 8, b, idesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&ctl.o_full);
+        } else {
+          mbar_arrive(&ctl.o_full);
+        }
+      }
+      ok = mbar_wait(&ctl.o_full, half, p.err, kErrWaitMma) && ok;
+      __syncwarp();
+      tc_fence_after();
+      if (direct) {
+        __nv_bfloat16* orow = p.out + ((int64_t)q * p.num_q_heads + h) * kDv + half * 256;
+#pragma unroll 1
+        for (int jj = 0; jj < 16; ++jj) {
+          float o[16];
+          tmem_ld16(lane_base + kColO + 16 * jj, o);
+          tmem_wait_ld();
+          if (row_valid) {
+            uint4 w0, w1;
+            w0.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+            w0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+            w0.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+            w0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+            w1.x = pack_bf16x2(o[8] * inv, o[9] * inv);
+            w1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
+            w1.z = pack_bf16x2(o[12] * inv, o[13] * inv);
+            w1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
+            uint4* dst = reinterpret_cast<uint4*>(orow + 16 * jj);
+            dst[0] = w0;
+            dst[1] = w1;
+          }
+        }
+      } else {
+        float* prow = p.part_o + (((int64_t)q * p.nslices + slice) * p.num_q_heads + h) * kDv +
+                      half * 256;
+#pragma unroll 1
+        for (int jj = 0; jj < 16; ++jj) {
+          float o[16];
+          tmem_ld16(lane_base + kColO + 16 * jj, o);
+          tmem_wait_ld();
+          if (row_valid) {
+            float4* dst = reinterpret_cast<float4*>(prow + 16 * jj);
+            dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+            dst[2] = make_float4(o[8], o[9], o[10], o[11]);
+            dst[3] = make_float4(o[12], o[13], o[14], o[15]);
+          }
         }
       }
     }
-  } else if (threadIdx.x == 0) {
-    // ---- MMA issuer: S = Q K^T over nine slabs ----------------------------
-    const uint32_t idesc = idesc_bf16(128, npad, false);
-    for (int j = 0; j < kNumQkSlabs && ok; ++j) {
-      const int st = j & 1;
-      const int use = j >> 1;
-      ok = mbar_wait(&ctl.step_full[st], use & 1, p.err, kErrWaitLoad);
-      const bool streamed = j < 5;
-      if (ok && !streamed) ok = mbar_wait(&ctl.res_full[j - 5], 0, p.err, kErrWaitLoad);
-      if (!ok) break;
-      tc_fence_after();
-      const uint8_t* kb = streamed ? s_kst + st * kSlabBytesK : s_res + (j - 5) * kSlabBytesK;
-      const uint8_t* qb = s_qst + st * kSlabBytesQ;
-#pragma unroll
-      for (int kk = 0; kk < kSlab / 16; ++kk) {
-        const uint64_t a = smem_desc(smem_u32(qb) + kk * 32, 16, 1024, kLayoutSw128);
-        const uint64_t b = smem_desc(smem_u32(kb) + kk * 32, 16, 1024, kLayoutSw128);
-        mma_ss(tmem + kColS, a, b, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+    if (row_valid) {
+      if (direct) p.lse[(int64_t)h * p.nq + q] = (m + log2f(l)) * kLn2;
+      if (p.part_ml) {
+        float* ml = p.part_ml + (((int64_t)q * p.nslices + slice) * p.num_q_heads + h) * 2;
+        ml[0] = m;
+        ml[1] = l;
       }
-      mma_commit(&ctl.step_empty[st]);
-    }
-    if (ok) mma_commit(&ctl.s_full);
-    else mbar_arrive(&ctl.s_full);
-  }
-
-  // ---- softmax over the slice's keys (thread = head row) -------------------
-  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-  ok = mbar_wait(&ctl.s_full, 0, p.err, kErrWaitMma) && ok;
-  __syncwarp();
-  tc_fence_after();
-  const float c2 = p.scale_log2;
-  const int nch = (npad + 31) >> 5;
-  float m = -INFINITY;
-  for (int c = 0; c < nch; ++c) {
-    float s[32];
-    tmem_ld32(lane_base + kColS + 32 * c, s);
-    tmem_wait_ld();
-    const int c0 = 32 * c;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) m = fmaxf(m, (c0 + e < n) ? s[e] * c2 : -INFINITY);
-  }
-  float l = 0.f;
-  for (int c = 0; c < nch; ++c) {
-    float s[32];
-    tmem_ld32(lane_base + kColS + 32 * c, s);
-    tmem_wait_ld();
-    const int c0 = 32 * c;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      s[e] = (c0 + e < n) ? ex2_approx(fmaf(s[e], c2, -m)) : 0.f;
-      l += s[e];
-    }
-    uint32_t pk[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(s[2 * e], s[2 * e + 1]);
-    tmem_st16(lane_base + kColS + 16 * c, pk);
-  }
-  tmem_wait_st();
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- O_half = P V --------------------------------------------------------
-  if (threadIdx.x == 0) {
-    tc_fence_after();
-    if (ok) {
-      const uint32_t idesc = idesc_bf16(128, 256, true);
-      for (int kk = 0; kk < npad / 16; ++kk) {
-        const uint64_t b = smem_desc(smem_u32(s_res) + kk * 16 * 128, kSlabBytesK, 1024,
-                                     kLayoutSw128);
-        mma_ts(tmem + kColO, tmem + kColS + kk * 8, b, idesc, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(&ctl.o_full);
-    } else {
-      mbar_arrive(&ctl.o_full);
-    }
-  }
-  mbar_wait(&ctl.o_full, 0, p.err, kErrWaitMma);
-  __syncwarp();
-  tc_fence_after();
-
-  // ---- epilogue --------------------------------------------------------------
-  if (direct) {
-    float den = l, alpha = 1.f;
-    if (MODE == SA_SINK_NULL_LOGIT) {
-      const float mp = fmaxf(m, sink2);
-      alpha = ex2_approx(m - mp);
-      den = l * alpha + ex2_approx(sink2 - mp);
-    }
-    const float inv = alpha / den;
-    __nv_bfloat16* orow = p.out + ((int64_t)q * p.num_q_heads + h) * kDv + half * 256;
-#pragma unroll 1
-    for (int j = 0; j < 16; ++j) {
-      float o[16];
-      tmem_ld16(lane_base + kColO + 16 * j, o);
-      tmem_wait_ld();
-      if (row_valid) {
-        uint4 w0, w1;
-        w0.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-        w0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-        w0.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-        w0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-        w1.x = pack_bf16x2(o[8] * inv, o[9] * inv);
-        w1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
-        w1.z = pack_bf16x2(o[12] * inv, o[13] * inv);
-        w1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
-        uint4* dst = reinterpret_cast<uint4*>(orow + 16 * j);
-        dst[0] = w0;
-        dst[1] = w1;
-      }
-    }
-    if (half == 0 && row_valid) p.lse[(int64_t)h * p.nq + q] = (m + log2f(l)) * kLn2;
-    if (p.part_ml && half == 0 && row_valid) {
-      float* ml = p.part_ml + (((int64_t)q * p.nslices + slice) * p.num_q_heads + h) * 2;
-      ml[0] = m;
-      ml[1] = l;
-    }
-  } else {
-    float* prow = p.part_o + (((int64_t)q * p.nslices + slice) * p.num_q_heads + h) * kDv +
-                  half * 256;
-#pragma unroll 1
-    for (int j = 0; j < 16; ++j) {
-      float o[16];
-      tmem_ld16(lane_base + kColO + 16 * j, o);
-      tmem_wait_ld();
-      if (row_valid) {
-        float4* dst = reinterpret_cast<float4*>(prow + 16 * j);
-        dst[0] = make_float4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_float4(o[4], o[5], o[6], o[7]);
-        dst[2] = make_float4(o[8], o[9], o[10], o[11]);
-        dst[3] = make_float4(o[12], o[13], o[14], o[15]);
-      }
-    }
-    if (half == 0 && row_valid) {
-      float* ml = p.part_ml + (((int64_t)q * p.nslices + slice) * p.num_q_heads + h) * 2;
-      ml[0] = m;
-      ml[1] = l;
     }
   }
 
   // ---- teardown ----------------------------------------------------------------
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 32 && !ok) {
-    // bounded drain of any gather still in flight
-    for (int r = 0; r < kHalfSlabs; ++r) mbar_wait(&ctl.res_full[r], 0, p.err, kErrWaitDrain);
-  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-// Merge the (O, m, l) partials of queries whose keys span several slices;
-// one CTA per (head, query), 128 threads x 4 V columns.
+// Merge the (O, m, l) partials of queries whose keys span several slices and
+// fold the sink once.  One CTA per (query, 4 heads): thread t takes head
+// t / 64 and V columns 8 (t mod 64) .. + 8, reading every slice's partial row
+// with independent 16-byte loads.
 template <int MODE>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(256)
 sparse_index_combine_kernel(const IndexParams p) {
   const int q = blockIdx.x;
-  const int h = blockIdx.y;
+  const int h = blockIdx.y * 4 + (threadIdx.x >> 6);
+  if (h >= p.num_q_heads) return;
+  const int d = (threadIdx.x & 63) * 8;
   const float* ml = p.part_ml + ((int64_t)q * p.nslices * p.num_q_heads + h) * 2;
   const int64_t ml_stride = (int64_t)p.num_q_heads * 2;
+  const float* base = p.part_o + ((int64_t)q * p.nslices * p.num_q_heads + h) * kDv + d;
+  const int64_t o_stride = (int64_t)p.num_q_heads * kDv;
+  // (m, l) of every slice first, all loads independent
+  float2 v[kMaxSlices];
+#pragma unroll
+  for (int s = 0; s < kMaxSlices; ++s)
+    v[s] = s < p.nslices ? *reinterpret_cast<const float2*>(ml + s * ml_stride)
+                         : make_float2(-INFINITY, 0.f);
   int nonempty = 0;
   float M = -INFINITY;
-  for (int s = 0; s < p.nslices; ++s) {
-    const float l = ml[s * ml_stride + 1];
-    if (l > 0.f) {
-      ++nonempty;
-      M = fmaxf(M, ml[s * ml_stride]);
-    }
+#pragma unroll
+  for (int s = 0; s < kMaxSlices; ++s) {
+    nonempty += v[s].y > 0.f ? 1 : 0;
+    M = v[s].y > 0.f ? fmaxf(M, v[s].x) : M;
   }
   if (nonempty < 2) return;  // finished by the slice kernel
   float L = 0.f;
-  for (int s = 0; s < p.nslices; ++s) {
-    const float l = ml[s * ml_stride + 1];
-    if (l > 0.f) L += l * ex2_approx(ml[s * ml_stride] - M);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  // partial rows in groups of eight slices, loads issued before use
+  for (int s0 = 0; s0 < p.nslices; s0 += 8) {
+    float4 o0[8], o1[8];
+    float w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int s = s0 + k;
+      float2 vs = make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int t = 0; t < kMaxSlices; ++t) vs = (t == s) ? v[t] : vs;
+      const bool live = s < p.nslices && vs.y > 0.f;
+      w[k] = live ? ex2_approx(vs.x - M) : 0.f;
+      L += live ? vs.y * w[k] : 0.f;
+      o0[k] = live ? *reinterpret_cast<const float4*>(base + s * o_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+      o1[k] = live ? *reinterpret_cast<const float4*>(base + s * o_stride + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      acc[0] = fmaf(w[k], o0[k].x, acc[0]);
+      acc[1] = fmaf(w[k], o0[k].y, acc[1]);
+      acc[2] = fmaf(w[k], o0[k].z, acc[2]);
+      acc[3] = fmaf(w[k], o0[k].w, acc[3]);
+      acc[4] = fmaf(w[k], o1[k].x, acc[4]);
+      acc[5] = fmaf(w[k], o1[k].y, acc[5]);
+      acc[6] = fmaf(w[k], o1[k].z, acc[6]);
+      acc[7] = fmaf(w[k], o1[k].w, acc[7]);
+    }
   }
   float den = L, alpha = 1.f;
   if (MODE == SA_SINK_NULL_LOGIT) {
@@ -450,38 +539,23 @@ sparse_index_combine_kernel(const IndexParams p) {
     den = L * alpha + ex2_approx(sink2 - mp);
   }
   const float inv = alpha / den;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int d = threadIdx.x * 4;
-  for (int s = 0; s < p.nslices; ++s) {
-    const float l = ml[s * ml_stride + 1];
-    if (!(l > 0.f)) continue;
-    const float w = ex2_approx(ml[s * ml_stride] - M);
-    const float4 o = *reinterpret_cast<const float4*>(
-        p.part_o + (((int64_t)q * p.nslices + s) * p.num_q_heads + h) * kDv + d);
-    acc.x = fmaf(w, o.x, acc.x);
-    acc.y = fmaf(w, o.y, acc.y);
-    acc.z = fmaf(w, o.z, acc.z);
-    acc.w = fmaf(w, o.w, acc.w);
-  }
-  uint2 packed;
-  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(p.out + ((int64_t)q * p.num_q_heads + h) * kDv + d) = packed;
-  if (threadIdx.x == 0) p.lse[(int64_t)h * p.nq + q] = (M + log2f(L)) * kLn2;
+  uint4 packed;
+  packed.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  packed.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  packed.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+  packed.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(p.out + ((int64_t)q * p.num_q_heads + h) * kDv + d) = packed;
+  if ((threadIdx.x & 63) == 0) p.lse[(int64_t)h * p.nq + q] = (M + log2f(L)) * kLn2;
 }
 
 template <int MODE>
 sa_status launch_typed(const IndexArgs& a, int nslices) {
-  CUtensorMap tq, tkv;
+  CUtensorMap tq;
   const uint64_t dq[2] = {(uint64_t)kDqk, (uint64_t)a.num_queries * a.num_q_heads};
   const uint64_t sq[1] = {(uint64_t)kDqk * 2};
   const uint32_t bq[2] = {kSlab, 128};
-  const uint64_t dk[2] = {(uint64_t)kDqk, (uint64_t)a.num_kv};
-  const uint32_t bk[2] = {kSlab, 1};
   if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, dq, sq, bq,
-                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tiled(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kv, dk, sq, bk,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+                    CU_TENSOR_MAP_SWIZZLE_128B))
     return SA_ERR_INVALID_ARG;
   IndexParams p;
   p.indices = a.indices;
@@ -507,14 +581,14 @@ sa_status launch_typed(const IndexArgs& a, int nslices) {
   if (e != cudaSuccess)
     return fail(SA_ERR_CUDA, "sa_sparse_index_fwd: %s", cudaGetErrorString(e));
   const int nhb = (a.num_q_heads + 127) / 128;
-  dim3 grid((unsigned)a.num_queries, (unsigned)(2 * nhb), (unsigned)nslices);
-  kern<<<grid, 128, smem, a.stream>>>(tq, tkv, p);
+  dim3 grid((unsigned)a.num_queries, (unsigned)nhb, (unsigned)nslices);
+  kern<<<grid, 256, smem, a.stream>>>(tq, reinterpret_cast<const uint16_t*>(a.kv), p);
   e = cudaGetLastError();
   if (e != cudaSuccess)
     return fail(SA_ERR_CUDA, "sa_sparse_index_fwd launch: %s", cudaGetErrorString(e));
   if (nslices > 1) {
-    dim3 g2((unsigned)a.num_queries, (unsigned)a.num_q_heads);
-    sparse_index_combine_kernel<MODE><<<g2, 128, 0, a.stream>>>(p);
+    dim3 g2((unsigned)a.num_queries, (unsigned)((a.num_q_heads + 3) / 4));
+    sparse_index_combine_kernel<MODE><<<g2, 256, 0, a.stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess)
       return fail(SA_ERR_CUDA, "sa_sparse_index_fwd combine launch: %s", cudaGetErrorString(e));
