@@ -120,8 +120,11 @@ SA_API sa_status sa_varlen_window_fwd(const void* q, const void* k, const void* 
  *   lse        fp32 [num_q_heads, num_queries]                 (written)
  *   workspace  device scratch of at least
  *              sa_sparse_index_workspace_size(num_queries, num_q_heads, dv, topk)
- *              bytes (may be NULL when that size is 0), 16-byte aligned; its
- *              contents need no initialisation and are overwritten.
+ *              bytes (may be NULL when that size is 0: no queries or topk = 0),
+ *              16-byte aligned; its contents need no initialisation and are
+ *              overwritten.  It holds the compacted index rows, the valid
+ *              count of each query and, when topk > 256, the split-KV partials
+ *              (O, m, l per query, 256-key item and head).
  * Supported: dqk = 576, dv = 512, topk <= 8192, num_kv < 2^31.
  */
 SA_API sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent,

@@ -4,7 +4,8 @@ Covers the full 64-query x 128-head decode workload with 1/4/16/128/512/2048
 valid keys per query (afierka-intel/vllm pull 76, Why / Test plan), the
 -inf no-op, empty rows, -1 padding anywhere in the row, out-of-range and
 repeated indices, lists that end inside a slice, head counts below and above
-one 128-row block, and workspace reuse across calls.
+one 128-row block, more than 256 queries, more than eight 256-key items per
+query, and workspace reuse across calls.
 """
 import numpy as np
 import pytest
@@ -123,3 +124,21 @@ def test_workspace_reuse_with_stale_contents():
     # second call: the multi-slice rows become single-slice and vice versa
     idx2 = c.indices[::-1].copy()
     check(c, NULL, indices=idx2, workspace=ws)
+
+
+@pytest.mark.parametrize("nq", [600, 1100])
+def test_many_queries(nq):
+    # more than 256 queries: each CTA's item lookup scans several queries
+    # per thread; full and short items of many queries interleave
+    c = W.index_case(nq, 16, 576, 512, 4096, 520, (0, 520, 7, 256, 300, 1),
+                     (-2.2, 2.49), NULL, 3400 + nq, "many_q")
+    check(c, NULL)
+
+
+@pytest.mark.parametrize("hq", [128, 40])
+def test_more_than_eight_items(hq):
+    # topk 3000: 2900 and 2100 valid keys give 12 and 9 items of 256 keys
+    # (the merge path for more than eight items), 300 gives 2, 7 gives 1
+    c = W.index_case(4, hq, 576, 512, 9000, 3000, (2900, 300, 2100, 7), (-2.2, 2.49),
+                     NULL, 3500 + hq, "many_items")
+    check(c, NULL)
