@@ -27,6 +27,26 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank,
 // Address of this device's error word (a __device__ variable).
 uint32_t* device_error_word();
 
+// Launch with programmatic stream serialisation: the kernel may begin while
+// the previous kernel of the stream finishes, and must call griddep_wait()
+// before its first global memory access that the previous kernel could
+// affect (every kernel here waits before any global access at all).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 struct WindowArgs {
   const void* q;
   const void* k;

@@ -963,25 +963,6 @@ sparse_index_combine_kernel(const IndexParams p) {
   }
 }
 
-// Launch with programmatic stream serialisation: the kernel may begin while
-// the previous kernel of the stream finishes; it calls griddep_wait() before
-// it reads that kernel's results.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                             cudaStream_t stream, Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
 struct WorkspaceLayout {
   size_t cidx, qcount, ml, o, total;
 };

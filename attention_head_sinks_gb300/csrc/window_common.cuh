@@ -21,6 +21,29 @@ namespace win {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Blackwell packed fp32 pair arithmetic (each lane rounded as the scalar
+// instruction) and the three-input maximum.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Largest b with cu[b] <= t (0 <= b < n), i.e. the sequence holding token t.
 __device__ __forceinline__ int find_seq(const int32_t* cu, int n, int t) {
   int lo = 0, hi = n - 1;
@@ -76,7 +99,7 @@ __device__ __forceinline__ RowMeta row_meta(const int32_t* cu, int num_seqs,
 
 template <int MODE>
 __device__ __forceinline__ void max_one(const float (&s)[32], int c, const RowMeta& r,
-                                        float c2, uint32_t span, float (&mr)[8], float& ms) {
+                                        float c2, uint32_t span, float (&mr)[4], float& ms) {
   const int c0 = 32 * c;
   const bool full = __all_sync(0xffffffffu, c0 >= r.clo && c0 + 31 <= r.chi);
   const bool has_k0 = (MODE == SA_SINK_KEY0_BIAS) &&
@@ -90,57 +113,69 @@ __device__ __forceinline__ void max_one(const float (&s)[32], int c, const RowMe
     }
   } else if (full) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) mr[e & 7] = fmaxf(mr[e & 7], s[e]);
+    for (int e = 0; e < 32; e += 2) mr[(e >> 1) & 3] = max3f(mr[(e >> 1) & 3], s[e], s[e + 1]);
   } else {
 #pragma unroll
-    for (int e = 0; e < 32; ++e)
-      mr[e & 7] = fmaxf(mr[e & 7], ((uint32_t)(c0 + e - r.clo) <= span) ? s[e] : -INFINITY);
+    for (int e = 0; e < 32; e += 2)
+      mr[(e >> 1) & 3] =
+          max3f(mr[(e >> 1) & 3], ((uint32_t)(c0 + e - r.clo) <= span) ? s[e] : -INFINITY,
+                ((uint32_t)(c0 + e + 1 - r.clo) <= span) ? s[e + 1] : -INFINITY);
   }
 }
 
 // P = 2^(x - m_use) as bf16 for one chunk (in registers s, stored to
-// p_addr + 16 c); adds the chunk's values to the partial sums lp.
+// p_addr + 16 c); adds the chunk's values to the partial pair sums lp.  The
+// exponent is fma(s, c2, -m) in every branch (pairs by the packed fma, each
+// lane rounded as the scalar one) and every branch accumulates in the same
+// order, so a zero KEY0_BIAS sink reproduces the no-sink bits exactly.
 template <int MODE>
 __device__ __forceinline__ void exp_one(float (&s)[32], int c, const RowMeta& r, float c2,
-                                        float m_use, uint32_t span, float (&lp)[8],
+                                        float m_use, uint32_t span, uint64_t (&lp)[4],
                                         uint32_t p_addr) {
   const int c0 = 32 * c;
   const bool full = __all_sync(0xffffffffu, c0 >= r.clo && c0 + 31 <= r.chi);
   const bool has_k0 = (MODE == SA_SINK_KEY0_BIAS) &&
                       __any_sync(0xffffffffu, r.ck0 >= c0 && r.ck0 < c0 + 32);
+  const uint64_t c2c2 = f2_pack(c2, c2), nmnm = f2_pack(-m_use, -m_use);
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const uint64_t t = f2_fma(f2_pack(s[e], s[e + 1]), c2c2, nmnm);
+    s[e] = f2_lo(t);
+    s[e + 1] = f2_hi(t);
+  }
   if (full && !has_k0) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) s[e] = ex2_approx(fmaf(s[e], c2, -m_use));
+    for (int e = 0; e < 32; ++e) s[e] = ex2_approx(s[e]);
   } else {
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      float x = fmaf(s[e], c2, -m_use);
+      float x = s[e];
       if (MODE == SA_SINK_KEY0_BIAS && c0 + e == r.ck0) x = x + r.sink2;
       s[e] = ((uint32_t)(c0 + e - r.clo) <= span) ? ex2_approx(x) : 0.f;
     }
   }
-#pragma unroll
-  for (int e = 0; e < 32; ++e) lp[e & 7] += s[e];
   uint32_t pk[16];
 #pragma unroll
-  for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(s[2 * e], s[2 * e + 1]);
+  for (int e = 0; e < 32; e += 2) {
+    lp[(e >> 1) & 3] = f2_add(lp[(e >> 1) & 3], f2_pack(s[e], s[e + 1]));
+    pk[e >> 1] = pack_bf16x2(s[e], s[e + 1]);
+  }
   tmem_st16(p_addr + 16 * c, pk);
 }
 
 // Max of the scaled (log2) logits of chunks [c_lo, c_hi].  Chunks without
 // the biased key take the max of the raw logits (scaling by c2 > 0 is
 // monotone, so max(s) * c2 == max(s * c2) exactly); the chunk holding the
-// biased key is scaled element by element.  Eight partial maxima keep the
-// dependency chains short.  Returns -inf when no element is live.
+// biased key is scaled element by element.  Four partial maxima of
+// three-input max operations keep the dependency chains short.  Returns
+// -inf when no element is live.
 template <int MODE, bool DB = true>
 __device__ __forceinline__ float max_chunks(uint32_t s_addr, int c_lo, int c_hi,
                                             const RowMeta& r, float c2) {
   float sa[32];
   [[maybe_unused]] float sb[DB ? 32 : 1];
   const uint32_t span = (uint32_t)(r.chi - r.clo);
-  float mr[8], ms = -INFINITY;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) mr[e] = -INFINITY;
+  float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, ms = -INFINITY;
   if constexpr (DB) {
     if (c_lo <= c_hi) {
       tmem_ld32(s_addr + 32 * c_lo, sa);
@@ -162,13 +197,12 @@ __device__ __forceinline__ float max_chunks(uint32_t s_addr, int c_lo, int c_hi,
       max_one<MODE>(sa, c, r, c2, span, mr, ms);
     }
   }
-  const float mraw = fmaxf(fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])),
-                           fmaxf(fmaxf(mr[4], mr[5]), fmaxf(mr[6], mr[7])));
+  const float mraw = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
   return fmaxf(mraw * c2, ms);
 }
 
 // P = 2^(x - m_use) as bf16 for chunks [c_lo, c_hi]; returns their row sum
-// (eight partial sums).  Every branch forms the exponent as fma(s, c2, -m)
+// (eight partial sums, kept as four packed pairs).  Every branch forms the exponent as fma(s, c2, -m)
 // (+ sink on key 0) so that a zero KEY0_BIAS sink reproduces the no-sink
 // bits exactly.
 template <int MODE, bool DB = true>
@@ -178,9 +212,7 @@ __device__ __forceinline__ float exp_chunks(uint32_t s_addr, uint32_t p_addr, in
   float sa[32];
   [[maybe_unused]] float sb[DB ? 32 : 1];
   const uint32_t span = (uint32_t)(r.chi - r.clo);
-  float lp[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) lp[e] = 0.f;
+  uint64_t lp[4] = {0, 0, 0, 0};
   if constexpr (DB) {
     if (c_lo <= c_hi) {
       tmem_ld32(s_addr + 32 * c_lo, sa);
@@ -202,7 +234,8 @@ __device__ __forceinline__ float exp_chunks(uint32_t s_addr, uint32_t p_addr, in
       exp_one<MODE>(sa, c, r, c2, m_use, span, lp, p_addr);
     }
   }
-  return ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
+  const uint64_t s = f2_add(f2_add(lp[0], lp[1]), f2_add(lp[2], lp[3]));
+  return f2_lo(s) + f2_hi(s);
 }
 
 // P = 0 for chunks [c_lo, c_hi].
@@ -216,11 +249,11 @@ __device__ __forceinline__ void zero_chunks(uint32_t p_addr, int c_lo, int c_hi)
 // Whole-row softmax over chunks [0, nchunks), the live ones being
 // [ch_lo, ch_hi].  Returns the row max m (log2 units, -inf for an empty row)
 // and the row sum l of 2^(x - m).
-template <int MODE, bool DB = true>
+template <int MODE, bool DB = true, bool DB_MAX = DB>
 __device__ __forceinline__ void softmax_rows(uint32_t s_addr, uint32_t p_addr, int nchunks,
                                              int ch_lo, int ch_hi, const RowMeta& r,
                                              float c2, float& m_out, float& l_out) {
-  const float m = max_chunks<MODE, DB>(s_addr, ch_lo, ch_hi, r, c2);
+  const float m = max_chunks<MODE, DB_MAX>(s_addr, ch_lo, ch_hi, r, c2);
   // Rows with no finite logit use 0 as the reference so that -inf - m stays -inf.
   const float m_use = (m == -INFINITY) ? 0.f : m;
   l_out = exp_chunks<MODE, DB>(s_addr, p_addr, ch_lo, ch_hi, r, c2, m_use);
