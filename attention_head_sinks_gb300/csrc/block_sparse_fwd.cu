@@ -20,7 +20,9 @@
 //   softmax over S_j with per-element selection / causal / document masks,
 //   P_j (bf16) written over S_j, O += P_j V_j with P_j read from TMEM.
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
-// warps 4..7 softmax and epilogue (warp w reads TMEM lanes 32 (w mod 4) ...).
+// warps 4..11 softmax and epilogue: warps w and w + 4 read TMEM lanes
+// 32 (w mod 4) ... and split each step's two blocks (and the O columns)
+// between them; each reads its 64 scores once per step.
 // The running max is rescaled lazily: O and l are rescaled only when a row's
 // max grows by more than 2^8, so P stays below 256.
 #include <cuda_bf16.h>
@@ -46,6 +48,7 @@ constexpr int kMaxBitmapWords = 512;           // 16384 blocks per batch row
 constexpr int kTmemCols = 512;
 constexpr int kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kThreads = 384;  // warps 0..3: roles; 4..7 and 8..11: softmax parts 0 and 1
 
 struct BlockParams {
   const int32_t* table;  // [T, topk]
@@ -72,11 +75,39 @@ struct __align__(8) BlockSmemCtl {
   uint64_t o_done;
   uint32_t tmem_base;
   int32_t nunion;
+  float red_m[2][2][128];  // [step parity][part][row]: row max exchange
+  float red_l[2][128];     // [part][row]: row sums at the end
   int32_t tok_pos[128];  // row-local position (-1 past the last token)
   int32_t tok_lo[128];   // row-local start of the token's document
   uint32_t bitmap[kMaxBitmapWords];
   int32_t prefix[kMaxBitmapWords];
 };
+
+// Blackwell packed fp32 pair arithmetic (each lane rounded as the scalar
+// instruction) and the three-input maximum.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ void bar_softmax() {  // the eight softmax warps
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
 
 __device__ __forceinline__ int upper_doc(const int32_t* cu, int n, int t) {
   int lo = 0, hi = n - 1;  // largest e with cu[e] <= t
@@ -88,7 +119,7 @@ __device__ __forceinline__ int upper_doc(const int32_t* cu, int n, int t) {
 }
 
 template <int G, int MODE>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
@@ -122,7 +153,7 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       ctl.tok_lo[tid] = 0;
     }
   }
-  for (int w = tid; w < nwords; w += 256) ctl.bitmap[w] = 0u;
+  for (int w = tid; w < nwords; w += kThreads) ctl.bitmap[w] = 0u;
   if (tid == 0) {
     mbar_init(&ctl.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
@@ -131,14 +162,14 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl.s_full[b], 1);
-      mbar_init(&ctl.p_full[b], 4);
+      mbar_init(&ctl.p_full[b], 8);
     }
     mbar_init(&ctl.o_done, 1);
     fence_mbar_init();
   }
   __syncthreads();
   const int npairs = TQ * p.topk;
-  for (int w = tid; w < npairs; w += 256) {
+  for (int w = tid; w < npairs; w += kThreads) {
     const int i = w / p.topk;
     const int pos = ctl.tok_pos[i];
     if (pos < 0) continue;
@@ -173,7 +204,7 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
   __syncthreads();
   const int U = ctl.nunion;
-  for (int w = tid; w < nwords; w += 256) {
+  for (int w = tid; w < nwords; w += kThreads) {
     uint32_t bits = ctl.bitmap[w];
     int o = ctl.prefix[w];
     while (bits) {
@@ -182,9 +213,9 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       ulist[o++] = w * 32 + b;
     }
   }
-  for (int w = tid; w < U * TW; w += 256) tokmask[w] = 0u;
+  for (int w = tid; w < U * TW; w += kThreads) tokmask[w] = 0u;
   __syncthreads();
-  for (int w = tid; w < npairs; w += 256) {
+  for (int w = tid; w < npairs; w += kThreads) {
     const int i = w / p.topk;
     const int pos = ctl.tok_pos[i];
     if (pos < 0) continue;
@@ -277,156 +308,170 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint8_t* vst = sKV + st * kStageBytes + 2 * kKVSlab;
       for (int kk = 0; kk < nb * kBlk / 16; ++kk) {
         const uint64_t b = smem_desc(smem_u32(vst) + kk * 16 * 128, kKVSlab, 1024, kLayoutSw128);
-        mma_ts(tmem + kColO, tmem + (uint32_t)(st * 128) + kk * 8, b, idesc,
+        // P of block kk / 4 sits in the first half of that block's S columns
+        mma_ts(tmem + kColO, tmem + (uint32_t)(st * 128 + 64 * (kk >> 2) + 8 * (kk & 3)), b, idesc,
                (j > 0 || kk > 0) ? 1u : 0u);
       }
       mma_commit(&ctl.kv_empty[st]);
       mma_commit(&ctl.o_done);
     }
   } else if (warp >= 4) {
-    // ---- softmax + epilogue (thread = row = TMEM lane) -----------------------
-    const int row = (warp - 4) * 32 + lane;
+    // ---- softmax + epilogue -------------------------------------------------
+    // Thread (row, part): row = TMEM lane, part = which of the step's two
+    // 64-key blocks it owns (S columns [64 part, 64 part + 64)); warps w and
+    // w + 4 share the 32 lanes of quadrant w mod 4.  The row max meets in
+    // shared memory once per step; each part keeps its own row sum.
+    const int part = (warp - 4) >> 2;
+    const int row = (warp & 3) * 32 + lane;
     const int tok = row / G;
     const int h = g * G + (row % G);
     const int t = tok0 + tok;
     const int pos = ctl.tok_pos[tok];
     const int dlo = ctl.tok_lo[tok];
-    const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const float c2 = p.scale_log2;
     float m_use = -INFINITY, l = 0.f;
 
     for (int j = 0; j < nsteps; ++j) {
       const int st = j & 1;
-      ok = mbar_wait(&ctl.s_full[st], (j >> 1) & 1, p.err, kErrWaitMma);
+      ok = mbar_wait(&ctl.s_full[st], (j >> 1) & 1, p.err, kErrWaitMma) && ok;
       __syncwarp();
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      const int nb = min(2, U - 2 * j);
-      // live column range per block: [clo, chi] (empty -> unreachable range)
-      int clo[2], chi[2];
-#pragma unroll
-      for (int bi = 0; bi < 2; ++bi) {
-        clo[bi] = 1 << 30;
-        chi[bi] = 1 << 30;
-        if (bi < nb && pos >= 0) {
-          const int u = 2 * j + bi;
-          if ((tokmask[u * TW + (tok >> 5)] >> (tok & 31)) & 1u) {
-            const int bs = ulist[u] * kBlk;
-            clo[bi] = max(dlo, bs) - bs;
-            chi[bi] = min(pos, bs + kBlk - 1) - bs;
-          }
-        }
+      // live columns of this thread's block: [clo, chi] within the block
+      const int u = 2 * j + part;
+      int clo = 1 << 30, chi = 1 << 30;
+      if (u < U && pos >= 0 && ((tokmask[u * TW + (tok >> 5)] >> (tok & 31)) & 1u)) {
+        const int bs = ulist[u] * kBlk;
+        clo = max(dlo, bs) - bs;
+        chi = min(pos, bs + kBlk - 1) - bs;
       }
-      const uint32_t sbase = lane_base + (uint32_t)(st * 128);
-      // pass 1: step max
+      const uint32_t span = (uint32_t)(chi - clo);
+      const bool warp_live = __any_sync(0xffffffffu, clo != (1 << 30));
+      const uint32_t sbase = lane_base + (uint32_t)(st * 128 + 64 * part);
+      float s[2][32];
       float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int bi = c >> 1;
-        const int c0 = (c & 1) * 32;
-        float s[32];
-        tmem_ld32(sbase + 32 * c, s);
+      if (warp_live) {
+        tmem_ld32(sbase, s[0]);
+        tmem_ld32(sbase + 32, s[1]);
         tmem_wait_ld();
-        const uint32_t span = (uint32_t)(chi[bi] - clo[bi]);
+        float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          mx = fmaxf(mx, ((uint32_t)(c0 + e - clo[bi]) <= span) ? s[e] * c2 : -INFINITY);
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            s[c][e] = ((uint32_t)(32 * c + e - clo) <= span) ? s[c][e] : -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            mr[(e >> 1) & 3] = max3f(mr[(e >> 1) & 3], s[c][e], s[c][e + 1]);
+        }
+        mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * c2;
       }
+      ctl.red_m[st][part][row] = mx;
+      bar_softmax();
+      mx = fmaxf(ctl.red_m[st][0][row], ctl.red_m[st][1][row]);
       // lazy rescale of O and l when this row's max grew by more than 2^8
       const bool need = mx > m_use + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mx : m_use;
         const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
         if (j > 0) {
-          ok = mbar_wait(&ctl.o_done, (j - 1) & 1, p.err, kErrWaitMma);
+          ok = mbar_wait(&ctl.o_done, (j - 1) & 1, p.err, kErrWaitMma) && ok;
           __syncwarp();
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < kD / 32; ++c) {
+          for (int c = 0; c < 2; ++c) {
             float o[32];
-            tmem_ld32(lane_base + kColO + 32 * c, o);
+            const uint32_t oa = lane_base + kColO + 64 * part + 32 * c;
+            tmem_ld32(oa, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(lane_base + kColO + 32 * c, o);
+            tmem_st32(oa, o);
           }
           tmem_wait_st();
           l *= alpha;
         }
         m_use = m_new;
       }
-      const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;
-      // pass 2: P = 2^(x - m) (bf16, in place), row sum
+      if (warp_live) {
+        // P = 2^(x - m) (bf16) into the first 32 columns of this block's S
+        // region, behind this thread's own reads; masked columns give 0
+        const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;
+        const uint64_t c2c2 = f2_pack(c2, c2), nmnm = f2_pack(-m_ref, -m_ref);
+        uint64_t lp[4] = {0, 0, 0, 0};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int bi = c >> 1;
-        const int c0 = (c & 1) * 32;
-        float s[32];
-        tmem_ld32(sbase + 32 * c, s);
-        tmem_wait_ld();
-        const uint32_t span = (uint32_t)(chi[bi] - clo[bi]);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          s[e] = ((uint32_t)(c0 + e - clo[bi]) <= span) ? ex2_approx(fmaf(s[e], c2, -m_ref)) : 0.f;
-          l += s[e];
+          for (int e = 0; e < 32; e += 2) {
+            const uint64_t x = f2_fma(f2_pack(s[c][e], s[c][e + 1]), c2c2, nmnm);
+            const float p0 = ex2_approx(f2_lo(x)), p1 = ex2_approx(f2_hi(x));
+            lp[(e >> 1) & 3] = f2_add(lp[(e >> 1) & 3], f2_pack(p0, p1));
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(sbase + 16 * c, pk);
         }
-        uint32_t pk[16];
+        const uint64_t ls = f2_add(f2_add(lp[0], lp[1]), f2_add(lp[2], lp[3]));
+        l += f2_lo(ls) + f2_hi(ls);
+      } else if (u < U) {
+        // block present for the tile but not for these rows: P = 0
+        uint32_t z[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(s[2 * e], s[2 * e + 1]);
-        tmem_st16(sbase + 16 * c, pk);
+        for (int e = 0; e < 16; ++e) z[e] = 0u;
+        tmem_st16(sbase, z);
+        tmem_st16(sbase + 16, z);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.p_full[st]);
     }
-    if (ok && nsteps > 0) {
-      ok = mbar_wait(&ctl.o_done, (nsteps - 1) & 1, p.err, kErrWaitMma);
+    if (nsteps > 0) {
+      ok = mbar_wait(&ctl.o_done, (nsteps - 1) & 1, p.err, kErrWaitMma) && ok;
       __syncwarp();
       tc_fence_after();
     }
-    // epilogue
+    ctl.red_l[part][row] = l;
+    bar_softmax();
+    const float lt = ctl.red_l[0][row] + ctl.red_l[1][row];
+    // epilogue: this thread stores O columns [64 part, 64 part + 64)
     float inv = 0.f, lse = -INFINITY;
     if (m_use != -INFINITY) {
-      float den = l, alpha = 1.f;
+      float den = lt, alpha = 1.f;
       if (MODE == SA_SINK_NULL_LOGIT) {
         const float sink2 = __ldg(p.sinks + h) * kLog2e;
         const float mp = fmaxf(m_use, sink2);
         alpha = ex2_approx(m_use - mp);
-        den = l * alpha + ex2_approx(sink2 - mp);
+        den = lt * alpha + ex2_approx(sink2 - mp);
       }
       inv = alpha / den;
-      lse = (m_use + log2f(l)) * kLn2;
+      lse = (m_use + log2f(lt)) * kLn2;
     }
     const bool row_valid = pos >= 0;
-    __nv_bfloat16* orow = p.out + ((int64_t)t * p.num_q_heads + h) * kD;
+    __nv_bfloat16* orow = p.out + ((int64_t)t * p.num_q_heads + h) * kD + 64 * part;
 #pragma unroll 1
-    for (int jj = 0; jj < kD / 16; ++jj) {
-      float o[16];
+    for (int c = 0; c < 2; ++c) {
+      float o[32];
       if (nsteps > 0) {
-        tmem_ld16(lane_base + kColO + 16 * jj, o);
+        tmem_ld32(lane_base + kColO + 64 * part + 32 * c, o);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) o[e] = 0.f;
+        for (int e = 0; e < 32; ++e) o[e] = 0.f;
       }
       if (row_valid) {
-        uint4 w0, w1;
-        w0.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-        w0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-        w0.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-        w0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-        w1.x = pack_bf16x2(o[8] * inv, o[9] * inv);
-        w1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
-        w1.z = pack_bf16x2(o[12] * inv, o[13] * inv);
-        w1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
-        uint4* dst = reinterpret_cast<uint4*>(orow + 16 * jj);
-        dst[0] = w0;
-        dst[1] = w1;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 w;
+          w.x = pack_bf16x2(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
+          w.y = pack_bf16x2(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
+          w.z = pack_bf16x2(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
+          w.w = pack_bf16x2(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
+          *reinterpret_cast<uint4*>(orow + 32 * c + 8 * q4) = w;
+        }
       }
     }
-    if (row_valid) p.lse[(int64_t)h * p.total_tokens + t] = lse;
+    if (row_valid && part == 0) p.lse[(int64_t)h * p.total_tokens + t] = lse;
   }
 
   // ---- teardown ----------------------------------------------------------------
@@ -479,7 +524,7 @@ sa_status launch_typed(const BlockArgs& a) {
   if (e != cudaSuccess)
     return fail(SA_ERR_CUDA, "sa_block_sparse_fwd: %s", cudaGetErrorString(e));
   dim3 grid((unsigned)(T / TQ), (unsigned)a.num_kv_heads);
-  kern<<<grid, 256, smem, a.stream>>>(tq, tk, tv, p);
+  kern<<<grid, kThreads, smem, a.stream>>>(tq, tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess)
     return fail(SA_ERR_CUDA, "sa_block_sparse_fwd launch: %s", cudaGetErrorString(e));
