@@ -143,6 +143,23 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int nwords = (p.nblocks + 31) >> 5;
 
   // ---- tile metadata: token positions, union of live blocks ---------------
+  // Every global read of the set-up is issued first (this thread's block-table
+  // entries, kept in registers for both passes below, and the document start
+  // of the tile's tokens); barrier set-up, the TMEM allocation and the Q load
+  // overlap them.
+  constexpr int kPairsPerThread = (kMaxUnion + kThreads - 1) / kThreads;
+  const int npairs = TQ * p.topk;  // <= kMaxUnion (checked on the host)
+  int32_t sel[kPairsPerThread];
+#pragma unroll
+  for (int k = 0; k < kPairsPerThread; ++k) {
+    const int w = tid + k * kThreads;
+    sel[k] = -1;
+    if (w < npairs) {
+      const int i = w / p.topk;
+      if (tok0 + i < p.total_tokens)
+        sel[k] = __ldg(p.table + (int64_t)(tok0 + i) * p.topk + (w - i * p.topk));
+    }
+  }
   if (tid < TQ) {
     const int t = tok0 + tid;
     if (t < p.total_tokens) {
@@ -166,16 +183,33 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     mbar_init(&ctl.o_done, 1);
     fence_mbar_init();
+    // Q of the tile does not depend on the key set: load it now
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+    mbar_arrive_expect_tx(&ctl.q_full, 2 * kQSlab);
+    for (int s2 = 0; s2 < 2; ++s2)
+      tma_load_3d(sQ + s2 * kQSlab, &tm_q, &ctl.q_full, 64 * s2, g * G, tok0);
+  }
+  if (warp == 2) {
+    tmem_alloc(&ctl.tmem_base, kTmemCols);
+    tmem_relinquish();
   }
   __syncthreads();
-  const int npairs = TQ * p.topk;
-  for (int w = tid; w < npairs; w += kThreads) {
-    const int i = w / p.topk;
+  // live selection of pair w = (token i, entry): block b intersects [doc start, pos]
+  auto live_block = [&](int k, int& i, int& b) -> bool {
+    const int w = tid + k * kThreads;
+    if (w >= npairs) return false;
+    i = w / p.topk;
+    b = sel[k];
     const int pos = ctl.tok_pos[i];
-    if (pos < 0) continue;
-    const int b = __ldg(p.table + (int64_t)(tok0 + i) * p.topk + (w - i * p.topk));
-    if (b >= 0 && b < p.nblocks && b * kBlk <= pos && b * kBlk + kBlk - 1 >= ctl.tok_lo[i])
-      atomicOr(&ctl.bitmap[b >> 5], 1u << (b & 31));
+    return pos >= 0 && b >= 0 && b < p.nblocks && b * kBlk <= pos &&
+           b * kBlk + kBlk - 1 >= ctl.tok_lo[i];
+  };
+#pragma unroll
+  for (int k = 0; k < kPairsPerThread; ++k) {
+    int i, b;
+    if (live_block(k, i, b)) atomicOr(&ctl.bitmap[b >> 5], 1u << (b & 31));
   }
   __syncthreads();
   if (warp == 0) {
@@ -215,20 +249,14 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
   for (int w = tid; w < U * TW; w += kThreads) tokmask[w] = 0u;
   __syncthreads();
-  for (int w = tid; w < npairs; w += kThreads) {
-    const int i = w / p.topk;
-    const int pos = ctl.tok_pos[i];
-    if (pos < 0) continue;
-    const int b = __ldg(p.table + (int64_t)(tok0 + i) * p.topk + (w - i * p.topk));
-    if (b >= 0 && b < p.nblocks && b * kBlk <= pos && b * kBlk + kBlk - 1 >= ctl.tok_lo[i]) {
+#pragma unroll
+  for (int k = 0; k < kPairsPerThread; ++k) {
+    int i, b;
+    if (live_block(k, i, b)) {
       const uint32_t word = ctl.bitmap[b >> 5];
       const int u = ctl.prefix[b >> 5] + __popc(word & ((1u << (b & 31)) - 1u));
       atomicOr(&tokmask[u * TW + (i >> 5)], 1u << (i & 31));
     }
-  }
-  if (warp == 2) {
-    tmem_alloc(&ctl.tmem_base, kTmemCols);
-    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -238,13 +266,7 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   bool ok = true;
 
   if (tid == 0 && nsteps > 0) {
-    // ---- producer ------------------------------------------------------------
-    tma_prefetch_map(&tm_q);
-    tma_prefetch_map(&tm_k);
-    tma_prefetch_map(&tm_v);
-    mbar_arrive_expect_tx(&ctl.q_full, 2 * kQSlab);
-    for (int s = 0; s < 2; ++s)
-      tma_load_3d(sQ + s * kQSlab, &tm_q, &ctl.q_full, 64 * s, g * G, tok0);
+    // ---- producer (Q was loaded during the set-up) ----------------------------
     int issued = 0;
     for (int j = 0; j < nsteps; ++j) {
       const int st = j & 1;
@@ -475,6 +497,8 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
 
   // ---- teardown ----------------------------------------------------------------
+  // a tile without live blocks never consumed its Q copy: let it land first
+  if (tid == 0 && nsteps == 0) mbar_wait(&ctl.q_full, 0, p.err, kErrWaitDrain);
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
