@@ -12,6 +12,7 @@ from ._lib import SAError, lib  # noqa: F401
 from .workloads import SINK_KEY0_BIAS, SINK_NONE, SINK_NULL_LOGIT  # noqa: F401
 
 __all__ = ["sa_varlen_window_fwd", "sa_sparse_index_fwd", "sa_block_sparse_fwd",
+           "sa_merge_attn_states",
            "sa_sparse_index_workspace_size", "sa_device_error", "sa_version", "SAError",
            "SINK_NONE", "SINK_KEY0_BIAS", "SINK_NULL_LOGIT"]
 
@@ -170,6 +171,39 @@ def sa_block_sparse_fwd(q, k, v, batch, seq_len, block_table, block_size,
         None if sinks is None else sinks.data_ptr(), int(sink_mode),
         float(softmax_scale), out.data_ptr(), lse.data_ptr(), None, 0,
         _stream_handle(stream)))
+    return out, lse
+
+
+def sa_merge_attn_states(out_a, lse_a, out_b, lse_b, sinks, sink_mode, out=None,
+                         lse=None, stream=None):
+    """Merge two sink-free partial results over disjoint key sets of the same
+    queries (C: ``sa_merge_attn_states``).
+
+    out_a/out_b bf16 ``[T,H,D]``, lse_a/lse_b fp32 ``[H,T]``; sinks fp32
+    ``[H]`` (or None with ``SINK_NONE``).  Returns ``(out, lse)`` (allocated
+    when not given; ``out`` may be ``out_a`` or ``out_b``).
+    """
+    torch = _torch()
+    _dev_tensor("out_a", out_a, torch.bfloat16, 3)
+    _dev_tensor("out_b", out_b, torch.bfloat16, 3)
+    _dev_tensor("lse_a", lse_a, torch.float32, 2)
+    _dev_tensor("lse_b", lse_b, torch.float32, 2)
+    T, h, d = out_a.shape
+    if out_b.shape != (T, h, d) or lse_a.shape != (h, T) or lse_b.shape != (h, T):
+        raise ValueError("partials must be out [T, H, D] and lse [H, T] of one shape")
+    if sinks is not None:
+        _dev_tensor("sinks", sinks, torch.float32, 1)
+    if out is None:
+        out = torch.empty_like(out_a)
+    if lse is None:
+        lse = torch.empty((h, T), dtype=torch.float32, device=out_a.device)
+    _dev_tensor("out", out, torch.bfloat16, 3)
+    _dev_tensor("lse", lse, torch.float32, 2)
+    from ._lib import check
+    check(lib().sa_merge_attn_states(
+        out_a.data_ptr(), lse_a.data_ptr(), out_b.data_ptr(), lse_b.data_ptr(), T, h, d,
+        None if sinks is None else sinks.data_ptr(), int(sink_mode), out.data_ptr(),
+        lse.data_ptr(), _stream_handle(stream)))
     return out, lse
 
 

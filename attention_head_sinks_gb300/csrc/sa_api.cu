@@ -317,4 +317,57 @@ sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent, int64_t num_
   return sa::launch_sparse_index_fwd(a);
 }
 
+sa_status sa_merge_attn_states(const void* out_a, const float* lse_a, const void* out_b,
+                               const float* lse_b, int64_t num_tokens, int32_t num_heads,
+                               int32_t head_dim, const float* sinks, int32_t sink_mode,
+                               void* out, float* lse, void* stream) {
+  const char* fn = "sa_merge_attn_states";
+  if (!out_a || !lse_a || !out_b || !lse_b || !out || !lse)
+    return fail(SA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (sink_mode < SA_SINK_NONE || sink_mode > SA_SINK_NULL_LOGIT)
+    return fail(SA_ERR_INVALID_ARG, "%s: unknown sink_mode %d", fn, sink_mode);
+  if (sink_mode == SA_SINK_NULL_LOGIT && !sinks)
+    return fail(SA_ERR_INVALID_ARG, "%s: sinks is NULL with sink_mode %d", fn, sink_mode);
+  if (num_tokens < 0 || num_heads < 1 || head_dim < 1)
+    return fail(SA_ERR_INVALID_ARG, "%s: bad sizes (num_tokens %lld, num_heads %d, head_dim %d)",
+                fn, (long long)num_tokens, num_heads, head_dim);
+  if (!sa::aligned(out_a, 16) || !sa::aligned(out_b, 16) || !sa::aligned(out, 16) ||
+      !sa::aligned(lse_a, 4) || !sa::aligned(lse_b, 4) || !sa::aligned(lse, 4) ||
+      (sinks && !sa::aligned(sinks, 4)))
+    return fail(SA_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  if (sink_mode == SA_SINK_KEY0_BIAS)
+    return fail(SA_ERR_UNSUPPORTED,
+                "%s: KEY0_BIAS lives in the partial holding key 0; merge with SA_SINK_NONE", fn);
+  if (head_dim % 8 != 0 || head_dim > 1024)
+    return fail(SA_ERR_UNSUPPORTED, "%s: head_dim %d (supported: multiples of 8 up to 1024)", fn,
+                head_dim);
+  {
+    // the merged LSE must not overlap an input LSE (a row's threads read the
+    // inputs while one of them writes the result)
+    const uintptr_t n = (uintptr_t)num_heads * (uintptr_t)num_tokens * sizeof(float);
+    const uintptr_t o = reinterpret_cast<uintptr_t>(lse);
+    for (const float* in : {lse_a, lse_b}) {
+      const uintptr_t i = reinterpret_cast<uintptr_t>(in);
+      if (n > 0 && o < i + n && i < o + n)
+        return fail(SA_ERR_INVALID_ARG, "%s: lse overlaps an input lse", fn);
+    }
+  }
+  if (num_tokens == 0) return SA_OK;
+  if (!sa::device_error_word()) return fail(SA_ERR_CUDA, "%s: no usable CUDA device", fn);
+  sa::MergeArgs a;
+  a.out_a = out_a;
+  a.lse_a = lse_a;
+  a.out_b = out_b;
+  a.lse_b = lse_b;
+  a.num_tokens = num_tokens;
+  a.num_heads = num_heads;
+  a.head_dim = head_dim;
+  a.sinks = sinks;
+  a.sink_mode = sink_mode;
+  a.out = out;
+  a.lse = lse;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return sa::launch_merge_states(a);
+}
+
 }  // extern "C"

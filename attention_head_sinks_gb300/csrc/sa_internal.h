@@ -125,4 +125,21 @@ struct BlockArgs {
 
 sa_status launch_block_sparse_fwd(const BlockArgs& a);
 
+struct MergeArgs {
+  const void* out_a;
+  const float* lse_a;
+  const void* out_b;
+  const float* lse_b;
+  int64_t num_tokens;
+  int32_t num_heads;
+  int32_t head_dim;
+  const float* sinks;
+  int32_t sink_mode;
+  void* out;
+  float* lse;
+  cudaStream_t stream;
+};
+
+sa_status launch_merge_states(const MergeArgs& a);
+
 }  // namespace sa

@@ -18,7 +18,8 @@ Workload shapes follow the pages:
 * sparse MLA decode with sinks in [-2.20, 2.49] and 1 ... 2048 valid keys per
   row (afierka-intel/vllm pull 76, Why);
 * DSA block-sparse prefill with document-packed rows (NeMo AutoModel
-  "minimax_m3_vl.cp_sparse_attn", MiniMaxM3CPSparseAttention).
+  "minimax_m3_vl.cp_sparse_attn", MiniMaxM3CPSparseAttention);
+* two partial results (output, LSE) to merge, shaped like the window block.
 """
 from __future__ import annotations
 
@@ -327,3 +328,40 @@ def dsa_block_prefill(mode=SINK_NULL_LOGIT, seed=1005, pad_rows=0,
     return block_case(2, 8192, 32, 4, 128, 64, 16, 3, (-2.2, 2.49), mode,
                       seed, pad_rows=pad_rows, name=tag,
                       sinks_neg_inf=sinks_neg_inf)
+
+
+# --------------------------------------------------------------------------
+# two partial attention results to merge (cascade over two key sets)
+# --------------------------------------------------------------------------
+@dataclasses.dataclass
+class MergeCase:
+    name: str
+    out_a: np.ndarray   # uint16 bf16 [T, H, D]
+    lse_a: np.ndarray   # float32 [H, T]
+    out_b: np.ndarray
+    lse_b: np.ndarray
+    sinks: np.ndarray   # float32 [H]
+    mode: int
+
+
+def merge_case(tokens, heads, dim, seed, lse_range=(-4.0, 6.0), empty_frac=0.05,
+               sink_range=(-2.2, 2.49), mode=SINK_NULL_LOGIT, name="merge") -> MergeCase:
+    """Two partials of ``tokens x heads`` rows of ``dim``: outputs N(0,1)
+    bf16, LSEs U[lse_range] with ``empty_frac`` of each set to -inf (a key
+    set with no keys; some rows get both), sinks U[sink_range]."""
+    rng = _rng(seed)
+    out_a = bf16_normal(rng, (tokens, heads, dim))
+    out_b = bf16_normal(rng, (tokens, heads, dim))
+    lse_a = rng.uniform(*lse_range, size=(heads, tokens)).astype(np.float32)
+    lse_b = rng.uniform(*lse_range, size=(heads, tokens)).astype(np.float32)
+    lse_a[rng.random((heads, tokens)) < empty_frac] = -np.inf
+    lse_b[rng.random((heads, tokens)) < empty_frac] = -np.inf
+    sinks = uniform_sinks(rng, heads, *sink_range)
+    return MergeCase(name, out_a, lse_a, out_b, lse_b, sinks, mode)
+
+
+def merge_window_partials(mode=SINK_NULL_LOGIT, seed=1006) -> MergeCase:
+    """The two partials of a cascade over the vision window block's shape:
+    16384 tokens x 16 heads x head dim 80."""
+    return merge_case(16384, 16, 80, seed, empty_frac=0.0, mode=mode,
+                      name="merge_window_16384tok")

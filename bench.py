@@ -67,6 +67,13 @@ class WindowRunner:
     # one-tile kernel in window_fwd.cu is the fallback for other shapes)
     source = "attention_head_sinks_gb300/csrc/window_ring_fwd.cu"
 
+
+    oracle_kind = "fp64 C oracle with OpenMP"
+    @staticmethod
+    def oracle_cores():
+        from oracle import sa_oracle
+        return sa_oracle.num_threads()
+
     def __init__(self, name):
         self.name = name
         if name == "vision_window_16384tok":
@@ -158,6 +165,13 @@ class IndexRunner:
     bound = "hbm"
     source = "attention_head_sinks_gb300/csrc/sparse_index_fwd.cu"
 
+
+    oracle_kind = "fp64 C oracle with OpenMP"
+    @staticmethod
+    def oracle_cores():
+        from oracle import sa_oracle
+        return sa_oracle.num_threads()
+
     def __init__(self, name):
         self.name = name
         self.c = W.mla_sparse_decode(W.SINK_NULL_LOGIT)
@@ -246,6 +260,13 @@ class BlockRunner:
     bound = "tensor"
     source = "attention_head_sinks_gb300/csrc/block_sparse_fwd.cu"
 
+
+    oracle_kind = "fp64 C oracle with OpenMP"
+    @staticmethod
+    def oracle_cores():
+        from oracle import sa_oracle
+        return sa_oracle.num_threads()
+
     def __init__(self, name):
         self.name = name
         self.c = W.dsa_block_prefill(W.SINK_NULL_LOGIT)
@@ -326,12 +347,91 @@ class BlockRunner:
                                    c.scale, rows=rows)
 
 
+class MergeRunner:
+    """sa_merge_attn_states on two window-block-shaped partials."""
+    bound = "hbm"
+
+    source = "attention_head_sinks_gb300/csrc/merge_states.cu"
+
+    oracle_kind = "fp64 NumPy oracle"
+    @staticmethod
+    def oracle_cores():
+        return 1  # the merge oracle is single-threaded NumPy
+
+    def __init__(self, name):
+        self.name = name
+        self.c = W.merge_window_partials(W.SINK_NULL_LOGIT)
+        self.mode = self.c.mode
+
+    def counts(self):
+        """Bytes: both partial outputs and LSEs read once, the merged output
+        and LSE written once.  Flops: 3 per output element (two scaled
+        terms and their sum)."""
+        c = self.c
+        T, h, d = c.out_a.shape
+        return 3 * T * h * d * 2 + 3 * h * T * 4, 3 * T * h * d
+
+    def config(self):
+        T, h, d = self.c.out_a.shape
+        return {"workload": self.name, "tokens": int(T), "heads": int(h), "head_dim": int(d),
+                "sink_mode": MODE_NAMES[self.mode]}
+
+    def setup(self, nsets):
+        import torch
+        c = self.c
+        dev = torch.device("cuda")
+        self.sets = []
+        for _ in range(nsets):
+            oa, ob = _torch_bits(c.out_a).to(dev), _torch_bits(c.out_b).to(dev)
+            la, lb = torch.from_numpy(c.lse_a).to(dev), torch.from_numpy(c.lse_b).to(dev)
+            out = torch.empty_like(oa)
+            lse = torch.empty_like(la)
+            self.sets.append((oa, la, ob, lb, out, lse))
+        self.sinks = torch.from_numpy(c.sinks).to(dev)
+
+    def touched_bytes(self):
+        return self.counts()[0]
+
+    def launches_per_call(self):
+        return 1
+
+    def call(self, i, mode=None):
+        import attention_head_sinks_gb300 as sa
+        oa, la, ob, lb, out, lse = self.sets[i % len(self.sets)]
+        sa.sa_merge_attn_states(oa, la, ob, lb, self.sinks,
+                                self.mode if mode is None else mode, out=out, lse=lse)
+
+    def host_io(self):
+        import torch
+        c = self.c
+        host_in = [_torch_bits(c.out_a), torch.from_numpy(c.lse_a), _torch_bits(c.out_b),
+                   torch.from_numpy(c.lse_b), torch.from_numpy(c.sinks)]
+        out, lse = self.sets[0][4], self.sets[0][5]
+
+        def run(dev_in):
+            import attention_head_sinks_gb300 as sa
+            sa.sa_merge_attn_states(dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[4],
+                                    self.mode, out=out, lse=lse)
+        return host_in, [out, lse], run
+
+    def oracle_rows(self):
+        return self.c.out_a.shape[0]
+
+    def oracle(self, rows):
+        from oracle import sa_oracle
+        c = self.c
+        b, e = rows
+        sa_oracle.merge_states(c.out_a[b:e], c.lse_a[:, b:e], c.out_b[b:e], c.lse_b[:, b:e],
+                               c.sinks, self.mode)
+
+
 RUNNERS = {
     "vision_window_16384tok": WindowRunner,
     "vision_window_4096tok": WindowRunner,
     "gqa_window_16384tok": WindowRunner,
     "mla_sparse_decode": IndexRunner,
     "dsa_block_prefill": BlockRunner,
+    "merge_window_16384tok": MergeRunner,
 }
 
 
@@ -451,10 +551,10 @@ def cpu_baseline(runner, budget_s=10.0):
     dt = sum(_oracle_time(runner, r) for r in spans)
     n = sum(e - s for s, e in spans)
     us = dt * 1e6 * total / n
-    return {"value": round(us, 1), "unit": "us/call", "cores": sa_oracle.num_threads(),
+    return {"value": round(us, 1), "unit": "us/call", "cores": runner.oracle_cores(),
             "kind": "oracle",
-            "sample": "%d of %d query rows in %d evenly spread spans (all heads), fp64 C "
-                      "oracle with OpenMP; scaled to one call" % (n, total, len(spans))}
+            "sample": "%d of %d query rows in %d evenly spread spans (all heads), %s; "
+                      "scaled to one call" % (n, total, len(spans), runner.oracle_kind)}
 
 
 def run_reference(args, rank):
@@ -480,7 +580,7 @@ def run_reference(args, rank):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "config": runner.config(),
         "cpu_baseline": {"value": round(us_call, 1), "unit": "us/call",
-                         "cores": sa_oracle.num_threads(), "kind": "oracle",
+                         "cores": runner.oracle_cores(), "kind": "oracle",
                          "sample": "each step %d of %d query rows (all heads), walking "
                                    "the call in order; value scaled to one call"
                                    % (per, total)},

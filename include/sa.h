@@ -181,6 +181,36 @@ SA_API sa_status sa_block_sparse_fwd(const void* q, const void* k, const void* v
                                      void* stream);
 
 /*
+ * Merge of two partial attention results over disjoint key sets of the same
+ * queries (a cascade / split of one key set over calls) into the attention
+ * over their union.  Each partial is the sink-free attention over its own
+ * keys (computed with SA_SINK_NONE) with its LSE; the merge weighs them by
+ * their LSEs -- the LSE convention of vLLM pull 49815, LSE paragraph -- and,
+ * with SA_SINK_NULL_LOGIT, folds the sink once as afierka-intel/vllm pull 76,
+ * Implementation does after its key loop (the sink joins the denominator
+ * only; the merged LSE stays over real keys; a -inf sink changes nothing).
+ * A partial with LSE = -inf holds no keys; if both do, out = 0, LSE = -inf.
+ * KEY0_BIAS is a bias on a real key, already inside the partial that holds
+ * that key: merge those partials with SA_SINK_NONE (KEY0_BIAS returns
+ * SA_ERR_UNSUPPORTED).
+ *
+ *   out_a, out_b  bf16 [num_tokens, num_heads, head_dim]
+ *   lse_a, lse_b  fp32 [num_heads, num_tokens]
+ *   out           bf16 [num_tokens, num_heads, head_dim]  (written; may be
+ *                 out_a or out_b itself)
+ *   lse           fp32 [num_heads, num_tokens]            (written; must not
+ *                 overlap lse_a or lse_b)
+ * Supported: head_dim a multiple of 8 and <= 1024; 16-byte aligned out
+ * pointers.  No workspace.
+ */
+SA_API sa_status sa_merge_attn_states(const void* out_a, const float* lse_a,
+                                      const void* out_b, const float* lse_b,
+                                      int64_t num_tokens, int32_t num_heads,
+                                      int32_t head_dim, const float* sinks,
+                                      int32_t sink_mode, void* out, float* lse,
+                                      void* stream);
+
+/*
  * Allocation-free variant of sa_sparse_index_fwd.  The pages have no
  * counterpart: it exists for callers that cannot allocate device memory for a
  * workspace -- for example code running inside a host runtime that owns the

@@ -141,3 +141,42 @@ def block_sparse_fwd(q, k, v, batch, seq_len, block_table, block_size,
     if rc != 0:
         raise ValueError("oracle_block_sparse_fwd rejected its arguments")
     return out, lse, cnt
+
+
+def _widen(a):
+    """bf16 bit patterns (uint16) to float64 exactly; other arrays as float64."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def merge_states(out_a, lse_a, out_b, lse_b, sinks, mode):
+    """Attention over the union of two disjoint key sets of the same queries,
+    from the two sink-free partial results (each the attention over its own
+    set, with its LSE): the LSE-weighted merge, with a NULL_LOGIT sink folded
+    once ([XPU sink] Implementation: the sink joins the denominator only, the
+    LSE stays over real keys; [MiMo sinks] LSE paragraph: LSE of the masked
+    scaled logits).  A partial with LSE = -inf has no keys; both empty gives
+    out = 0, LSE = -inf.
+
+    out_* ``[T,H,D]`` (bf16 bits as uint16, or float), lse_* ``[H,T]``.
+    Returns out ``[T,H,D]`` and lse ``[H,T]`` as float64.
+    """
+    oa, ob = _widen(out_a), _widen(out_b)
+    la = np.asarray(lse_a, np.float64).T[:, :, None]  # [T,H,1]
+    lb = np.asarray(lse_b, np.float64).T[:, :, None]
+    M = np.maximum(la, lb)
+    empty = M == -np.inf
+    Mr = np.where(empty, 0.0, M)
+    wa = np.exp(la - Mr)
+    wb = np.exp(lb - Mr)
+    Z = wa + wb
+    with np.errstate(divide="ignore"):
+        lse = np.where(empty, -np.inf, Mr + np.log(np.where(empty, 1.0, Z)))
+    den = Z
+    if mode == NULL_LOGIT:
+        s = np.asarray(sinks, np.float64)[None, :, None]
+        den = Z + np.exp(s - Mr)
+    out = np.where(empty, 0.0, (wa * oa + wb * ob) / np.where(empty, 1.0, den))
+    return out, lse[:, :, 0].T.copy()

@@ -167,3 +167,30 @@ def test_block_sparse_rejects_bad_arguments(lib, kw, status, needle):
 
 def test_block_sparse_empty_batch_is_a_no_op(lib):
     assert _block_call(lib, batch=0) == 0
+
+
+def _merge_call(lib, **kw):
+    a = dict(oa=16, la=16, ob=16, lb=16, T=100, H=4, D=80, sinks=16, mode=2, out=16,
+             lse=4096)
+    a.update(kw)
+    return lib.sa_merge_attn_states(a["oa"], a["la"], a["ob"], a["lb"], a["T"], a["H"],
+                                    a["D"], a["sinks"], a["mode"], a["out"], a["lse"], None)
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(oa=None), 1, "NULL"),
+    (dict(mode=7), 1, "sink_mode"),
+    (dict(sinks=None), 1, "sinks is NULL"),
+    (dict(H=0), 1, "bad sizes"),
+    (dict(out=24), 1, "misaligned"),
+    (dict(lse=16), 1, "overlaps"),
+    (dict(mode=1), 2, "KEY0_BIAS"),
+    (dict(D=12), 2, "head_dim"),
+])
+def test_merge_rejects_bad_arguments(lib, kw, status, needle):
+    assert _merge_call(lib, **kw) == status
+    assert needle in lib.sa_last_error().decode()
+
+
+def test_merge_empty_is_a_no_op(lib):
+    assert _merge_call(lib, T=0) == 0
