@@ -8,7 +8,9 @@
 // _local_sparse_forward.  Key set of token i (row position p, document start
 // d): { j in i's batch row : block(j) selected by i, d <= j <= p }.  The sink
 // follows afierka-intel/vllm pull 76, Implementation (folded after the key
-// loop, LSE over real keys only).
+// loop, LSE over real keys only).  KEY0_BIAS adds s_h to the logit of the first
+// key of the token's document (vLLM pull 49815, second paragraph, with
+// documents as the sequences), when that key is in the token's set.
 //
 // Tile: M = 128 rows = (128 / G) consecutive tokens x the G query heads of
 // one KV head (row = token * G + head).  Keys: the union, over the tile's
@@ -79,6 +81,7 @@ struct __align__(8) BlockSmemCtl {
   float red_l[2][128];     // [part][row]: row sums at the end
   int32_t tok_pos[128];  // row-local position (-1 past the last token)
   int32_t tok_lo[128];   // row-local start of the token's document
+  int32_t tok_k0[128];   // KEY0_BIAS key: row-local document start, -1 if before the row
   uint32_t bitmap[kMaxBitmapWords];
   int32_t prefix[kMaxBitmapWords];
 };
@@ -163,11 +166,14 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (tid < TQ) {
     const int t = tok0 + tid;
     if (t < p.total_tokens) {
+      const int doc = upper_doc(p.cu_docs, p.num_docs, t);
       ctl.tok_pos[tid] = t - row_start;
-      ctl.tok_lo[tid] = max(upper_doc(p.cu_docs, p.num_docs, t) - row_start, 0);
+      ctl.tok_lo[tid] = max(doc - row_start, 0);
+      ctl.tok_k0[tid] = doc >= row_start ? doc - row_start : -1;
     } else {
       ctl.tok_pos[tid] = -1;
       ctl.tok_lo[tid] = 0;
+      ctl.tok_k0[tid] = -1;
     }
   }
   for (int w = tid; w < nwords; w += kThreads) ctl.bitmap[w] = 0u;
@@ -352,6 +358,7 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int dlo = ctl.tok_lo[tok];
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const float c2 = p.scale_log2;
+    const float k0_sink2 = (MODE == SA_SINK_KEY0_BIAS) ? __ldg(p.sinks + h) * kLog2e : 0.f;
     float m_use = -INFINITY, l = 0.f;
 
     for (int j = 0; j < nsteps; ++j) {
@@ -362,31 +369,51 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       // live columns of this thread's block: [clo, chi] within the block
       const int u = 2 * j + part;
       int clo = 1 << 30, chi = 1 << 30;
+      int k0c = -1;  // KEY0_BIAS: column of the document's first key in this block
       if (u < U && pos >= 0 && ((tokmask[u * TW + (tok >> 5)] >> (tok & 31)) & 1u)) {
         const int bs = ulist[u] * kBlk;
         clo = max(dlo, bs) - bs;
         chi = min(pos, bs + kBlk - 1) - bs;
+        if (MODE == SA_SINK_KEY0_BIAS) {
+          const int k0 = ctl.tok_k0[tok];
+          if (k0 >= bs && k0 < bs + kBlk) k0c = k0 - bs;  // then k0c == clo: live
+        }
       }
+      const bool has_k0 = MODE == SA_SINK_KEY0_BIAS && __any_sync(0xffffffffu, k0c >= 0);
       const uint32_t span = (uint32_t)(chi - clo);
       const bool warp_live = __any_sync(0xffffffffu, clo != (1 << 30));
       const uint32_t sbase = lane_base + (uint32_t)(st * 128 + 64 * part);
       float s[2][32];
       float mx = -INFINITY;
+      float sk0 = -INFINITY;  // raw logit of the KEY0_BIAS key (taken out of s)
       if (warp_live) {
         tmem_ld32(sbase, s[0]);
         tmem_ld32(sbase + 32, s[1]);
         tmem_wait_ld();
         float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (has_k0) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            s[c][e] = ((uint32_t)(32 * c + e - clo) <= span) ? s[c][e] : -INFINITY;
+            for (int e = 0; e < 32; ++e) {
+              sk0 = (32 * c + e == k0c) ? s[c][e] : sk0;
+              s[c][e] = ((uint32_t)(32 * c + e - clo) <= span && 32 * c + e != k0c) ? s[c][e]
+                                                                                    : -INFINITY;
+            }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              s[c][e] = ((uint32_t)(32 * c + e - clo) <= span) ? s[c][e] : -INFINITY;
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
             mr[(e >> 1) & 3] = max3f(mr[(e >> 1) & 3], s[c][e], s[c][e + 1]);
-        }
-        mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * c2;
+        // max(s) * c2 == max(s * c2) exactly; the biased key enters scaled
+        mx = fmaxf(fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * c2, sk0 * c2 + k0_sink2);
       }
       ctl.red_m[st][part][row] = mx;
       bar_softmax();
@@ -420,6 +447,9 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         // region, behind this thread's own reads; masked columns give 0
         const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;
         const uint64_t c2c2 = f2_pack(c2, c2), nmnm = f2_pack(-m_ref, -m_ref);
+        // the biased key's exponent: fma(s, c2, -m) + sink (bitwise the no-sink
+        // value for a zero sink)
+        const float xk0 = fmaf(sk0, c2, -m_ref) + k0_sink2;
         uint64_t lp[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -427,7 +457,12 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const uint64_t x = f2_fma(f2_pack(s[c][e], s[c][e + 1]), c2c2, nmnm);
-            const float p0 = ex2_approx(f2_lo(x)), p1 = ex2_approx(f2_hi(x));
+            float x0 = f2_lo(x), x1 = f2_hi(x);
+            if (has_k0) {
+              x0 = (32 * c + e == k0c) ? xk0 : x0;
+              x1 = (32 * c + e + 1 == k0c) ? xk0 : x1;
+            }
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             lp[(e >> 1) & 3] = f2_add(lp[(e >> 1) & 3], f2_pack(p0, p1));
             pk[e >> 1] = pack_bf16x2(p0, p1);
           }
@@ -558,6 +593,7 @@ sa_status launch_typed(const BlockArgs& a) {
 template <int G>
 sa_status by_mode(const BlockArgs& a) {
   if (a.sink_mode == SA_SINK_NULL_LOGIT) return launch_typed<G, SA_SINK_NULL_LOGIT>(a);
+  if (a.sink_mode == SA_SINK_KEY0_BIAS) return launch_typed<G, SA_SINK_KEY0_BIAS>(a);
   return launch_typed<G, SA_SINK_NONE>(a);
 }
 

@@ -222,8 +222,6 @@ sa_status sa_block_sparse_fwd(const void* q, const void* k, const void* v, int32
       !sa::aligned(out, 16) || !sa::aligned(lse, 4) || !sa::aligned(cu_docs, 4) ||
       (block_table && !sa::aligned(block_table, 4)) || (sinks && !sa::aligned(sinks, 4)))
     return fail(SA_ERR_INVALID_ARG, "%s: misaligned pointer (bf16 tensors need 16 bytes)", fn);
-  if (sink_mode == SA_SINK_KEY0_BIAS)
-    return fail(SA_ERR_UNSUPPORTED, "%s: KEY0_BIAS is not supported on the block path", fn);
   if ((int64_t)batch * seq_len == 0) return SA_OK;
   if (!sa::device_error_word())
     return fail(SA_ERR_CUDA, "%s: no usable CUDA device", fn);

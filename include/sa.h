@@ -154,8 +154,10 @@ SA_API size_t sa_sparse_index_workspace_size(int32_t num_queries,
  * Block ids count blocks from the start of the batch row; ids outside
  * [0, seq_len / block_size) (the -1 padding) are absent; a repeated id is one
  * selection.  One selection per token is shared by all heads.  A row with an
- * empty key set gives zero output and LSE = -inf.  NONE and NULL_LOGIT are
- * supported; KEY0_BIAS returns SA_ERR_UNSUPPORTED.
+ * empty key set gives zero output and LSE = -inf.  NONE, NULL_LOGIT and
+ * KEY0_BIAS are supported; KEY0_BIAS adds s_h to the logit of the first token
+ * of the token's document (vLLM pull 49815, second paragraph, with documents
+ * as the sequences) when that key is in the token's set.
  *
  *   q            bf16 [batch * seq_len, num_q_heads, head_dim]
  *   k, v         bf16 [batch * seq_len, num_kv_heads, head_dim]

@@ -152,11 +152,21 @@ def block_sparse_fwd(q, k, v, batch, seq_len, block_table, block_size,
     T, hq, d = qf.shape
     hkv = kf.shape[1]
     mask = block_mask(batch, seq_len, block_table, block_size, cu_docs)
+    # KEY0_BIAS key of token i: the first token of its document, if that lies
+    # in i's batch row
+    cd = np.asarray(cu_docs, np.int64)
+    first_key = np.full(T, -1, np.int64)
+    for e in range(len(cd) - 1):
+        first_key[cd[e]:cd[e + 1]] = cd[e]
+    same_row = (first_key // seq_len) == (np.arange(T) // seq_len)
     out = np.zeros((T, hq, d))
     lse = np.zeros((hq, T))
     for h in range(hq):
         g = h // (hq // hkv)
         logits = scale * (qf[:, h, :] @ kf[:, g, :].T)
+        if mode == KEY0_BIAS:
+            rows = np.nonzero(same_row)[0]
+            logits[rows, first_key[rows]] += float(sinks[h])
         o, l = masked_softmax_attention(
             logits, mask, vf[:, g, :],
             float(sinks[h]) if mode == NULL_LOGIT else None)

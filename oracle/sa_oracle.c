@@ -31,7 +31,8 @@
  * The definition implemented, per query row i and query head h with key set
  * K(i) and kv head g = h / (Hq / Hkv):
  *     l_j   = scale * <q[i,h,:], k[j,g,:]>                       j in K(i)
- *     KEY0_BIAS:  l_j += s_h   for j = first key of i's sequence, if j in K(i)
+ *     KEY0_BIAS:  l_j += s_h   for j = first key of i's sequence (window) or
+ *                 document (block), if j in K(i)
  *     M     = max_j l_j,   Z = sum_j exp(l_j - M),   LSE = M + ln Z
  *     den   = Z e^M                    (NONE, KEY0_BIAS)
  *           = Z e^M + e^{s_h}          (NULL_LOGIT; LSE unchanged)
@@ -239,6 +240,8 @@ static int cmp_i32(const void* a, const void* b) {
 /* starts over the flattened tokens.  Key set of token i (row position p):  */
 /*   { j in i's batch row : (j's row position)/block in table(i),           */
 /*     j <= i, doc(j) == doc(i) }.                                          */
+/* KEY0_BIAS key: the first token of i's document (the [P1] bias on each    */
+/* sequence's first key, with documents as the sequences), if in the row.   */
 /* out [B*S,Hq,D]; lse [Hq,B*S]; key_count [B*S] (keys per token).          */
 /* ------------------------------------------------------------------------ */
 int oracle_block_sparse_fwd(const uint16_t* q, const uint16_t* k,
@@ -254,7 +257,6 @@ int oracle_block_sparse_fwd(const uint16_t* q, const uint16_t* k,
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || block_size <= 0 ||
       topk_blocks < 0 || batch < 0 || seq_len < 0)
     return -1;
-  if (mode == OR_KEY0_BIAS) return -1;
   if (num_docs < 1 || cu_docs[0] != 0 || cu_docs[num_docs] != T) return -1;
   if (row_begin < 0) row_begin = 0;
   if (row_end > T) row_end = T;
@@ -279,6 +281,9 @@ int oracle_block_sparse_fwd(const uint16_t* q, const uint16_t* k,
       int e = 0;
       while (e + 1 < num_docs && cu_docs[e + 1] <= i) ++e;
       const int64_t doc0 = cu_docs[e];
+      /* KEY0_BIAS key: the first token of i's document, when it lies in
+         i's batch row (a key of another row is never in the set) */
+      const int64_t bias_key = doc0 >= row0 ? doc0 : -1;
       /* selected blocks of i as a sorted set */
       int nsel = 0, t;
       for (t = 0; t < topk_blocks; ++t) {
@@ -306,7 +311,7 @@ int oracle_block_sparse_fwd(const uint16_t* q, const uint16_t* k,
         const double s = (mode == OR_NONE) ? 0.0 : (double)sinks[h];
         double l;
         attend_row(qrow, d, d, k + (int64_t)g * d, (int64_t)hkv * d,
-                   v + (int64_t)g * d, (int64_t)hkv * d, keys, n, -1, mode, s,
+                   v + (int64_t)g * d, (int64_t)hkv * d, keys, n, bias_key, mode, s,
                    scale, out + (i * hq + h) * (int64_t)d, &l, logit);
         lse[(int64_t)h * T + i] = l;
       }

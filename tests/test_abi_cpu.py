@@ -158,7 +158,6 @@ def _block_call(lib, **kw):
     (dict(hq=30), 1, "multiple"),
     (dict(batch=1 << 20), 1, "2^31"),
     (dict(out=8), 1, "misaligned"),
-    (dict(mode=1), 2, "KEY0_BIAS"),
 ])
 def test_block_sparse_rejects_bad_arguments(lib, kw, status, needle):
     assert _block_call(lib, **kw) == status

@@ -2,9 +2,10 @@
 
 Covers the full 2 x 8192-token workload (32 query / 4 KV heads, head dim 128,
 64-key blocks, top-16 blocks, 3 documents per batch row) on sampled rows in
-both sink variants, the padded-row variant (empty key sets), the -inf no-op,
-and small ragged cases over every GQA ratio with repeated, out-of-range and
-future block ids and document boundaries inside blocks.
+all three sink modes (KEY0_BIAS: the document's first key), the padded-row
+variant (empty key sets), the -inf and zero-bias no-ops, and small ragged
+cases over every GQA ratio with repeated, out-of-range and future block ids
+and document boundaries inside blocks.
 """
 import numpy as np
 import pytest
@@ -15,7 +16,7 @@ from tests.gpu_util import LSE_TOL, REL_L2_TOL, compare, dev
 
 pytestmark = pytest.mark.gpu
 
-NONE, NULL = W.SINK_NONE, W.SINK_NULL_LOGIT
+NONE, KEY0, NULL = W.SINK_NONE, W.SINK_KEY0_BIAS, W.SINK_NULL_LOGIT
 
 
 @pytest.fixture(autouse=True)
@@ -80,7 +81,7 @@ def check_sampled(c, mode, sinks=None):
     return out, lse
 
 
-@pytest.mark.parametrize("mode", [NULL, NONE])
+@pytest.mark.parametrize("mode", [NULL, NONE, KEY0])
 def test_dsa_block_prefill_full_size_sampled(mode):
     check_sampled(W.dsa_block_prefill(mode), mode)
 
@@ -114,7 +115,7 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("mode", [NULL, NONE])
+@pytest.mark.parametrize("mode", [NULL, NONE, KEY0])
 @pytest.mark.parametrize("ci", range(len(SMALL)))
 def test_small_ragged(ci, mode):
     batch, S, hq, hkv, topk, docs = SMALL[ci]
@@ -145,3 +146,12 @@ def test_all_rows_empty():
     tab = np.full_like(c.block_table, -1)
     out, lse = gpu_run(c, NULL, table=tab)
     assert (out == 0).all() and bool(lse.isneginf().all())
+
+
+def test_zero_key0_sink_is_bitwise_no_sink():
+    import torch
+    c = W.dsa_block_prefill(KEY0, seed=1405)
+    o0, l0 = gpu_run(c, NONE)
+    o1, l1 = gpu_run(c, KEY0, sinks=np.zeros_like(c.sinks))
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16))
+    assert torch.equal(l0, l1)

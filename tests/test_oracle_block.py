@@ -1,5 +1,9 @@
 """Pins of the block-sparse oracle.
 
+KEY0_BIAS on this path adds s_h to the logit of the first key of each
+token's document (vLLM pull 49815, second paragraph, with documents as the
+sequences), when that key is in the token's set.
+
 Source: NeMo AutoModel "nemo_automodel.components.models.minimax_m3_vl.
 cp_sparse_attn" -- MiniMaxM3CPSparseAttention step 4 (block selection +
 token-level causal), _local_sparse_forward (packed document masks, zero output
@@ -15,7 +19,7 @@ from oracle import brute
 from oracle import sa_oracle as O
 from tests.oracle_pins_util import bits_to_f64, expand_kv, rel_l2, sdpa_with_bias
 
-NONE, NULL = W.SINK_NONE, W.SINK_NULL_LOGIT
+NONE, KEY0, NULL = W.SINK_NONE, W.SINK_KEY0_BIAS, W.SINK_NULL_LOGIT
 
 
 def tiny(seed=41, pad_rows=0, docs=2, topk=3):
@@ -31,7 +35,7 @@ def run(c, mode, sinks=None, table=None, cu_docs=None, rows=None):
         c.sinks if sinks is None else sinks, mode, c.scale, rows=rows)
 
 
-@pytest.mark.parametrize("mode", [NONE, NULL])
+@pytest.mark.parametrize("mode", [NONE, KEY0, NULL])
 @pytest.mark.parametrize("pad", [0, 5])
 def test_brute_force_matches_set_enumeration(mode, pad):
     c = tiny(pad_rows=pad)
@@ -147,3 +151,48 @@ def test_dsa_generator_table_properties():
     cu = W.document_cuts(rng, 2, 8192, 3)
     assert len(cu) == 7 and cu[0] == 0 and cu[3] == 8192 and cu[-1] == 16384
     assert np.all(np.diff(cu) > 0)
+
+
+def test_key0_closed_form_correction():
+    """The vLLM pull 49815 correction applied to a no-sink run, with the
+    document's first token as key 0: p0 = exp(logit0 - lse), out' = (out +
+    p0 (e^s - 1) v0) / (1 + p0 (e^s - 1)), lse' = lse + ln(1 + p0 (e^s - 1))
+    on the rows whose set holds that key; the other rows are bit-identical."""
+    c = tiny(docs=3, topk=4)
+    o_none, l_none, _ = run(c, NONE)
+    o_k0, l_k0, _ = run(c, KEY0)
+    qf, kf, vf = bits_to_f64(c.q), bits_to_f64(c.k), bits_to_f64(c.v)
+    T, hq = c.total_tokens, c.num_q_heads
+    grp = hq // c.num_kv_heads
+    cd = c.cu_docs.astype(np.int64)
+    tab = c.block_table
+    nb = c.seq_len // c.block_size
+    reached = 0
+    for i in range(T):
+        e = int(np.searchsorted(cd, i, side="right") - 1)
+        k0 = int(cd[e])
+        row0 = (i // c.seq_len) * c.seq_len
+        b0 = (k0 - row0) // c.block_size
+        in_set = k0 >= row0 and any(0 <= b < nb and b == b0 for b in tab[i])
+        for h in range(hq):
+            g = h // grp
+            if in_set:
+                logit0 = c.scale * float(qf[i, h] @ kf[k0, g])
+                p0 = np.exp(logit0 - l_none[h, i])
+                es = np.expm1(float(c.sinks[h]))
+                corr = (o_none[i, h] + p0 * es * vf[k0, g]) / (1 + p0 * es)
+                assert np.allclose(o_k0[i, h], corr, rtol=1e-10, atol=1e-12)
+                assert abs(l_k0[h, i] - (l_none[h, i] + np.log1p(p0 * es))) < 1e-10
+                reached += 1
+            else:
+                assert np.array_equal(o_k0[i, h], o_none[i, h])
+                assert l_k0[h, i] == l_none[h, i] or (np.isneginf(l_k0[h, i]) and
+                                                      np.isneginf(l_none[h, i]))
+    assert reached > 0
+
+
+def test_key0_zero_sink_is_bitwise_no_sink():
+    c = tiny(docs=3, topk=4)
+    o0, l0, _ = run(c, NONE)
+    o1, l1, _ = run(c, KEY0, sinks=np.zeros_like(c.sinks))
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
