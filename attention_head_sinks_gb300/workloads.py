@@ -365,3 +365,81 @@ def merge_window_partials(mode=SINK_NULL_LOGIT, seed=1006) -> MergeCase:
     16384 tokens x 16 heads x head dim 80."""
     return merge_case(16384, 16, 80, seed, empty_frac=0.0, mode=mode,
                       name="merge_window_16384tok")
+
+
+# --------------------------------------------------------------------------
+# fp8 (e4m3) latent cache for the MLA decode
+# --------------------------------------------------------------------------
+def _e4m3_table():
+    """Positive e4m3 codes 0..126 (0x7F is NaN) and their values, ascending."""
+    codes = np.arange(127, dtype=np.int64)
+    e, m = codes >> 3, codes & 7
+    vals = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    return codes, vals
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 code (ties to the even code), saturating at +-448."""
+    codes, vals = _e4m3_table()
+    a = np.minimum(np.abs(np.asarray(x, np.float64)), 448.0)
+    i = np.clip(np.searchsorted(vals, a), 1, len(vals) - 1)
+    lo, hi = vals[i - 1], vals[i]
+    up = (a - lo > hi - a) | ((a - lo == hi - a) & (codes[i] % 2 == 0))
+    c = np.where(up, codes[i], codes[i - 1])
+    return (c | np.where(np.signbit(np.asarray(x)), 0x80, 0)).astype(np.uint8)
+
+
+@dataclasses.dataclass
+class IndexFp8Case:
+    name: str
+    q: np.ndarray          # uint16 bf16 [Nq, Hq, dqk]
+    kv: np.ndarray         # uint8 e4m3 codes [nkv, dqk]
+    kv_scale: np.ndarray   # float32 [nkv]: row value = code value x scale
+    indices: np.ndarray    # int32 [Nq, topk], -1 padded
+    dv: int
+    sinks: np.ndarray
+    mode: int
+    scale: float
+
+    @property
+    def num_queries(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def num_q_heads(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
+    def num_kv(self) -> int:
+        return int(self.kv.shape[0])
+
+    @property
+    def topk(self) -> int:
+        return int(self.indices.shape[1])
+
+
+def index_fp8_case(nq, hq, dqk, dv, nkv, topk, counts, sink_range, mode, seed,
+                   name="sparse_index_fp8", pow2_scales=False) -> IndexFp8Case:
+    """Latent rows N(0,1) quantised per row to e4m3 with scale amax / 448
+    (rounded to a power of two with ``pow2_scales``)."""
+    rng = _rng(seed)
+    q = bf16_normal(rng, (nq, hq, dqk))
+    rows = rng.standard_normal(size=(nkv, dqk), dtype=np.float32)
+    sinks = uniform_sinks(rng, hq, *sink_range)
+    indices = causal_topk_indices(rng, nq, nkv, topk, counts)
+    amax = np.abs(rows).max(axis=1).astype(np.float64)
+    scale = amax / 448.0
+    if pow2_scales:
+        scale = 2.0 ** np.round(np.log2(scale))
+    scale = scale.astype(np.float32)
+    kv = f32_to_e4m3_bits(rows / scale[:, None].astype(np.float64))
+    return IndexFp8Case(name, q, kv, scale, np.ascontiguousarray(indices, np.int32), dv,
+                        sinks, mode, float(np.float32(1.0 / math.sqrt(dqk))))
+
+
+def mla_sparse_decode_fp8(mode=SINK_NULL_LOGIT, seed=1007, num_kv=65536) -> IndexFp8Case:
+    """The MLA decode batch over an e4m3 latent cache with one fp32 scale per
+    row: 64 queries x 128 heads, qk dim 576, v dim 512, 65536 rows, top-2048
+    with 1/4/16/128/512/2048 valid entries cycled, sinks U[-2.20, 2.49]."""
+    return index_fp8_case(64, 128, 576, 512, num_kv, 2048, MLA_VALID_COUNTS,
+                          (-2.20, 2.49), mode, seed, "mla_sparse_decode_fp8_64q")

@@ -180,3 +180,51 @@ def merge_states(out_a, lse_a, out_b, lse_b, sinks, mode):
         den = Z + np.exp(s - Mr)
     out = np.where(empty, 0.0, (wa * oa + wb * ob) / np.where(empty, 1.0, den))
     return out, lse[:, :, 0].T.copy()
+
+
+def e4m3_to_f64(codes):
+    """Exact value of e4m3 codes (sign, 4-bit exponent with bias 7, 3-bit
+    mantissa; exponent 0 is subnormal; 0x7F / 0xFF are NaN)."""
+    c = np.asarray(codes, np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, c & 7
+    v = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    v = np.where((c & 0x7F) == 0x7F, np.nan, v)
+    return s * v
+
+
+def sparse_index_fwd_fp8(q, kv, kv_scale, indices, dv, sinks, mode, scale, rows=None):
+    """Top-k index attention into an e4m3 latent cache: latent row r is
+    ``e4m3(kv[r]) * kv_scale[r]`` (fp64), K the whole row, V its first ``dv``
+    columns; otherwise as ``sparse_index_fwd`` (afierka-intel/vllm pull 76,
+    Implementation: the listed keys exactly, NULL_LOGIT in the denominator
+    only, LSE over the listed keys).  q ``[Nq,Hq,dqk]`` as bf16 bits.
+    Returns out ``[Nq,Hq,dv]``, lse ``[Hq,Nq]`` float64 and the valid-key count.
+    """
+    qf = _widen(q)
+    nq, hq, dqk = qf.shape
+    nkv = kv.shape[0]
+    idx = np.asarray(indices, np.int64)
+    b, e = (0, nq) if rows is None else rows
+    out = np.full((nq, hq, dv), np.nan)
+    lse = np.full((hq, nq), np.nan)
+    cnt = np.full((nq,), -1, np.int32)
+    sk = np.asarray(sinks, np.float64) if sinks is not None else np.zeros(hq)
+    for i in range(b, e):
+        keys = idx[i][(idx[i] >= 0) & (idx[i] < nkv)]
+        cnt[i] = len(keys)
+        if len(keys) == 0:
+            out[i] = 0.0
+            lse[:, i] = -np.inf
+            continue
+        rows_f = e4m3_to_f64(kv[keys]) * np.asarray(kv_scale, np.float64)[keys][:, None]
+        logits = float(scale) * (qf[i] @ rows_f.T)          # [hq, n]
+        m = logits.max(axis=1, keepdims=True)
+        w = np.exp(logits - m)
+        z = w.sum(axis=1, keepdims=True)
+        lse[:, i] = (m + np.log(z))[:, 0]
+        den = z * np.exp(m)
+        if mode == NULL_LOGIT:
+            den = den + np.exp(sk)[:, None]
+        out[i] = (np.exp(logits) @ rows_f[:, :dv]) / den
+    return out, lse, cnt
