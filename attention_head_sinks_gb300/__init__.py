@@ -11,7 +11,8 @@ from __future__ import annotations
 from ._lib import SAError, lib  # noqa: F401
 from .workloads import SINK_KEY0_BIAS, SINK_NONE, SINK_NULL_LOGIT  # noqa: F401
 
-__all__ = ["sa_varlen_window_fwd", "sa_sparse_index_fwd", "sa_block_sparse_fwd",
+__all__ = ["sa_varlen_window_fwd", "sa_sparse_index_fwd", "sa_sparse_index_fwd_fp8",
+           "sa_block_sparse_fwd",
            "sa_merge_attn_states",
            "sa_sparse_index_workspace_size", "sa_device_error", "sa_version", "SAError",
            "SINK_NONE", "SINK_KEY0_BIAS", "SINK_NULL_LOGIT"]
@@ -124,6 +125,53 @@ def sa_sparse_index_fwd(q, kv_latent, indices, dv, sinks, sink_mode,
     from ._lib import check
     check(lib().sa_sparse_index_fwd(
         q.data_ptr(), kv_latent.data_ptr(), nkv, dqk, int(dv),
+        indices.data_ptr(), topk, nq, hq,
+        None if sinks is None else sinks.data_ptr(), int(sink_mode),
+        float(softmax_scale), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes,
+        _stream_handle(stream)))
+    return out, lse
+
+
+def sa_sparse_index_fwd_fp8(q, kv_fp8, kv_scale, indices, dv, sinks, sink_mode,
+                            softmax_scale, out=None, lse=None, workspace=None,
+                            stream=None):
+    """``sa_sparse_index_fwd`` over an e4m3 latent cache with one fp32 scale
+    per row (C: ``sa_sparse_index_fwd_fp8``).
+
+    kv_fp8 ``[nkv,dqk]`` e4m3 codes (uint8 or torch.float8_e4m3fn), kv_scale
+    fp32 ``[nkv]``: row r is ``e4m3(kv_fp8[r]) * kv_scale[r]``.  Everything
+    else as ``sa_sparse_index_fwd``.
+    """
+    torch = _torch()
+    if isinstance(kv_fp8, torch.Tensor) and kv_fp8.dtype == torch.float8_e4m3fn:
+        kv_fp8 = kv_fp8.view(torch.uint8)
+    _dev_tensor("q", q, torch.bfloat16, 3)
+    _dev_tensor("kv_fp8", kv_fp8, torch.uint8, 2)
+    _dev_tensor("kv_scale", kv_scale, torch.float32, 1)
+    _dev_tensor("indices", indices, torch.int32, 2)
+    nq, hq, dqk = q.shape
+    nkv = kv_fp8.shape[0]
+    topk = indices.shape[1]
+    if kv_fp8.shape[1] != dqk or indices.shape[0] != nq or kv_scale.shape[0] != nkv:
+        raise ValueError("kv_fp8 must be [nkv, dqk], kv_scale [nkv] and indices [Nq, topk]")
+    if sinks is not None:
+        _dev_tensor("sinks", sinks, torch.float32, 1)
+    if out is None:
+        out = torch.empty((nq, hq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((hq, nq), dtype=torch.float32, device=q.device)
+    need = sa_sparse_index_workspace_size(nq, hq, dv, topk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _dev_tensor("out", out, torch.bfloat16, 3)
+    _dev_tensor("lse", lse, torch.float32, 2)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _dev_tensor("workspace", workspace, torch.uint8, 1)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    from ._lib import check
+    check(lib().sa_sparse_index_fwd_fp8(
+        q.data_ptr(), kv_fp8.data_ptr(), kv_scale.data_ptr(), nkv, dqk, int(dv),
         indices.data_ptr(), topk, nq, hq,
         None if sinks is None else sinks.data_ptr(), int(sink_mode),
         float(softmax_scale), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes,

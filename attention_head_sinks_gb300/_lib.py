@@ -30,6 +30,9 @@ SIGNATURES = {
     "sa_sparse_index_fwd": (ctypes.c_int, [
         _P, _P, _I64, _I32, _I32, _P, _I32, _I32, _I32, _P, _I32, _F32, _P, _P,
         _P, _SZ, _P]),
+    "sa_sparse_index_fwd_fp8": (ctypes.c_int, [
+        _P, _P, _P, _I64, _I32, _I32, _P, _I32, _I32, _I32, _P, _I32, _F32, _P,
+        _P, _P, _SZ, _P]),
     "sa_sparse_index_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "sa_sparse_index_fwd_noalloc": (ctypes.c_int, [
         _P, _P, _I64, _I32, _I32, _P, _I32, _I32, _I32, _P, _I32, _F32, _P, _P,

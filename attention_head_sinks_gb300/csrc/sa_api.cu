@@ -254,14 +254,15 @@ size_t sa_sparse_index_workspace_size(int32_t num_queries, int32_t num_q_heads,
   return sa::sparse_index_workspace_bytes(num_queries, num_q_heads, topk);
 }
 
-sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent, int64_t num_kv,
-                              int32_t dqk, int32_t dv, const int32_t* indices,
-                              int32_t topk, int32_t num_queries, int32_t num_q_heads,
-                              const float* sinks, int32_t sink_mode, float softmax_scale,
-                              void* out, float* lse, void* workspace,
-                              size_t workspace_bytes, void* stream) {
-  const char* fn = "sa_sparse_index_fwd";
-  if (!q || !kv_latent || !indices || !out || !lse)
+namespace {
+// Shared checks and dispatch of the bf16 and fp8 latent-cache entry points.
+sa_status sparse_index_entry(const char* fn, const void* q, const void* kv_latent,
+                             const float* kv_scale, bool fp8, int64_t num_kv, int32_t dqk,
+                             int32_t dv, const int32_t* indices, int32_t topk,
+                             int32_t num_queries, int32_t num_q_heads, const float* sinks,
+                             int32_t sink_mode, float softmax_scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !kv_latent || !indices || !out || !lse || (fp8 && !kv_scale))
     return fail(SA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
   if (sink_mode < SA_SINK_NONE || sink_mode > SA_SINK_NULL_LOGIT)
     return fail(SA_ERR_INVALID_ARG, "%s: unknown sink_mode %d", fn, sink_mode);
@@ -276,7 +277,7 @@ sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent, int64_t num_
     return fail(SA_ERR_INVALID_ARG, "%s: softmax_scale must be finite and > 0", fn);
   if (!sa::aligned(q, 16) || !sa::aligned(kv_latent, 16) || !sa::aligned(out, 16) ||
       !sa::aligned(lse, 4) || !sa::aligned(indices, 4) || (sinks && !sa::aligned(sinks, 4)) ||
-      (workspace && !sa::aligned(workspace, 16)))
+      (workspace && !sa::aligned(workspace, 16)) || (kv_scale && !sa::aligned(kv_scale, 4)))
     return fail(SA_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
   if (sink_mode == SA_SINK_KEY0_BIAS)
     return fail(SA_ERR_UNSUPPORTED, "%s: KEY0_BIAS needs a sequence start; an index list has none",
@@ -297,6 +298,9 @@ sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent, int64_t num_
   sa::IndexArgs a;
   a.q = q;
   a.kv = kv_latent;
+  a.kv_scale = fp8 ? kv_scale : nullptr;
+  a.fp8 = fp8;
+  a.fn = fn;
   a.num_kv = num_kv;
   a.dqk = dqk;
   a.dv = dv;
@@ -313,6 +317,29 @@ sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent, int64_t num_
   a.workspace_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   return sa::launch_sparse_index_fwd(a);
+}
+}  // namespace
+
+sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent, int64_t num_kv,
+                              int32_t dqk, int32_t dv, const int32_t* indices,
+                              int32_t topk, int32_t num_queries, int32_t num_q_heads,
+                              const float* sinks, int32_t sink_mode, float softmax_scale,
+                              void* out, float* lse, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return sparse_index_entry("sa_sparse_index_fwd", q, kv_latent, nullptr, false, num_kv, dqk,
+                            dv, indices, topk, num_queries, num_q_heads, sinks, sink_mode,
+                            softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+sa_status sa_sparse_index_fwd_fp8(const void* q, const void* kv_fp8, const float* kv_scale,
+                                  int64_t num_kv, int32_t dqk, int32_t dv,
+                                  const int32_t* indices, int32_t topk, int32_t num_queries,
+                                  int32_t num_q_heads, const float* sinks, int32_t sink_mode,
+                                  float softmax_scale, void* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return sparse_index_entry("sa_sparse_index_fwd_fp8", q, kv_fp8, kv_scale, true, num_kv, dqk,
+                            dv, indices, topk, num_queries, num_q_heads, sinks, sink_mode,
+                            softmax_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 sa_status sa_merge_attn_states(const void* out_a, const float* lse_a, const void* out_b,

@@ -79,7 +79,10 @@ int num_sms();
 
 struct IndexArgs {
   const void* q;
-  const void* kv;
+  const void* kv;          // bf16 rows, or e4m3 rows when fp8
+  const float* kv_scale;   // fp8: fp32 scale per row (else null)
+  bool fp8;
+  const char* fn;          // entry-point name for error messages
   int64_t num_kv;
   int32_t dqk;
   int32_t dv;

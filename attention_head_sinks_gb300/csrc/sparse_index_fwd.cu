@@ -97,6 +97,7 @@ struct PlanParams {
 };
 
 struct IndexParams {
+  const float* kv_scale;  // fp8 cache: fp32 scale per latent row (else null)
   const int32_t* cidx;    // compacted index rows [nq, topk]
   const int32_t* qcount;  // valid keys per query
   int32_t topk;
@@ -136,6 +137,9 @@ struct IndexRed {
   float m[2][128];
   float l[2][128];
 };
+// fp8 cache: the item's 256 row scales follow the reductions
+constexpr int kScaleOffset = (int)sizeof(IndexRed);
+static_assert(kScaleOffset % 16 == 0 && kScaleOffset + kItemKeys * 4 <= kSlabBytesQ, "");
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -299,6 +303,78 @@ __device__ void find_item(const IndexParams& p, int item, IndexSmemCtl& ctl) {
   __syncthreads();
 }
 
+// fp8 cache: 8-byte asynchronous copy (zero-filled when src_bytes is 0).
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// Eight e4m3 values (byte i = column i) as bf16 pairs.  Every e4m3 value is a
+// bf16 value, and e4m3 -> f16 -> f32 -> bf16 is exact at each step.
+__device__ __forceinline__ uint4 e4m3x8_to_bf16(uint2 raw) {
+  uint32_t h[4];
+  asm("{\n\t.reg .b16 a0, a1, a2, a3;\n\t"
+      "mov.b32 {a0, a1}, %4;\n\t"
+      "mov.b32 {a2, a3}, %5;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, a1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %2, a2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %3, a3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(raw.x), "r"(raw.y));
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+    o[i] = pack_bf16x2(f.x, f.y);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// fp8 cache, stage 1: the 64 e4m3 columns of slab `slab` of the slice's rows
+// go, 8 bytes per (row, chunk c), into the upper half of the 32 KB slot at
+// dst (row r at dst + 16 KB + 64 r); rows past n are zero-filled.
+__device__ __forceinline__ void stage_slab_fp8(uint32_t dst, const uint8_t* kv8,
+                                               const int32_t* kidx, int iters, int n, int r0,
+                                               int c, int slab) {
+#pragma unroll 4
+  for (int k = 0; k < iters; ++k) {
+    const int r = r0 + 16 * k;
+    const bool live = r < n;
+    const uint8_t* src = kv8 + (live ? (int64_t)kidx[r] * kDqk + slab * kSlab + c * 8 : 0);
+    cp_async8(dst + kItemKeys * 64 + r * 64 + c * 8, src, live ? 8u : 0u);
+  }
+}
+
+// fp8 cache, stage 2 (after the staged copies landed): read this thread's
+// staged chunks, wait for every gatherer (bf16 rows 128.. overwrite the
+// staging half), then write the values as bf16 into the slot's
+// 128-byte-swizzled [npad][64] layout.  The row scales are not applied here:
+// the softmax multiplies them into the logits and into P.
+__device__ __forceinline__ void convert_slab_fp8(uint32_t dst, int iters, int r0, int c) {
+  uint2 raw[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    if (k < iters) {
+      const uint32_t a = dst + kItemKeys * 64 + (r0 + 16 * k) * 64 + c * 8;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(raw[k].x), "=r"(raw[k].y) : "r"(a));
+    }
+  }
+  bar_gather();
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    if (k < iters) {
+      const int r = r0 + 16 * k;
+      const uint4 v = e4m3x8_to_bf16(raw[k]);
+      const uint32_t a = dst + r * 128 + ((c ^ (r & 7)) << 4);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+                   "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
+  }
+}
+
 // Gather 16-byte chunk c of slab `slab` of rows r0, r0 + 16, ... (< npad) into
 // the 128-byte-swizzled [npad][64] slot at dst; rows past n are zero-filled.
 __device__ __forceinline__ void gather_slab(uint32_t dst, const uint16_t* kv,
@@ -313,10 +389,13 @@ __device__ __forceinline__ void gather_slab(uint32_t dst, const uint16_t* kv,
   }
 }
 
-template <int MODE>
+template <int MODE, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const uint16_t* kv,
+sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv_raw,
                         const IndexParams p) {
+  // bf16 cache: rows of 576 bf16; fp8 cache: rows of 576 e4m3 bytes
+  const uint16_t* kv = reinterpret_cast<const uint16_t*>(kv_raw);
+  const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(kv_raw);
   extern __shared__ uint8_t smem_raw[];
   __shared__ IndexSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -373,21 +452,31 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const uint16_t
     const int gt = tid - 128;
     const int gr0 = (gt >> 3) & 15, gc = gt & 7;
     const int iters = npad >> 4;
+    float ks0 = 0.f, ks1 = 0.f;
     if (warp >= 4) {
       const int32_t* crow = p.cidx + (int64_t)q * p.topk + slice * kItemKeys;
       const int32_t i0 = gt < n ? __ldcg(crow + gt) : 0;
       const int32_t i1 = gt + 128 < n ? __ldcg(crow + gt + 128) : 0;
       ctl.kidx[gt] = i0;
       ctl.kidx[gt + 128] = i1;
+      if (FP8) {  // stored once S is complete (they go where Q was staged)
+        ks0 = gt < n ? __ldg(p.kv_scale + i0) : 0.f;
+        ks1 = gt + 128 < n ? __ldg(p.kv_scale + i1) : 0.f;
+      }
       bar_gather();
     }
 
     if (warp >= 4) {
       auto gather = [&](int slot, int slab) {
-        if (ok) gather_slab(slot_u32(slot), kv, ctl.kidx, iters, n, gr0, gc, slab);
+        if (ok) {
+          if (FP8) stage_slab_fp8(slot_u32(slot), kv8, ctl.kidx, iters, n, gr0, gc, slab);
+          else gather_slab(slot_u32(slot), kv, ctl.kidx, iters, n, gr0, gc, slab);
+        }
         cp_async_commit();
       };
-      auto publish = [&](uint64_t* bar) {
+      // the slot's copies have landed: (fp8: convert it, then) hand it over
+      auto publish_slot = [&](uint64_t* bar, int slot) {
+        if (FP8) convert_slab_fp8(slot_u32(slot), iters, gr0, gc);
         fence_proxy_async();
         mbar_arrive(bar);
       };
@@ -400,35 +489,40 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const uint16_t
       // the ring refills (slabs 5, 6, 7) wait for free slots: start their
       // DRAM reads now so that the copies find them in L2
       for (int r = gt; r < n; r += 128) {
-        const uint16_t* row = kv + (int64_t)ctl.kidx[r] * kDqk;
-        prefetch_l2(row + 5 * kSlab);
-        prefetch_l2(row + 6 * kSlab);
-        prefetch_l2(row + 7 * kSlab);
+        const int64_t row = (int64_t)ctl.kidx[r] * kDqk;
+        if (FP8) {
+          prefetch_l2(kv8 + row + 5 * kSlab);
+          prefetch_l2(kv8 + row + 7 * kSlab);
+        } else {
+          prefetch_l2(kv + row + 5 * kSlab);
+          prefetch_l2(kv + row + 6 * kSlab);
+          prefetch_l2(kv + row + 7 * kSlab);
+        }
       }
       cp_async_wait<5>();
-      publish(&ctl.kst_full[0]);
+      publish_slot(&ctl.kst_full[0], 4);
       cp_async_wait<4>();
-      publish(&ctl.kst_full[1]);
+      publish_slot(&ctl.kst_full[1], 5);
       cp_async_wait<3>();
-      publish(&ctl.res_full[0]);
+      publish_slot(&ctl.res_full[0], 0);
       if (ok) ok = mbar_wait(&ctl.kst_empty[0], 0, p.err, kErrWaitFree);  // step 0 done
       gather(4, 5);  // G6
       cp_async_wait<3>();
-      publish(&ctl.res_full[1]);
+      publish_slot(&ctl.res_full[1], 1);
       if (ok) ok = mbar_wait(&ctl.kst_empty[1], 0, p.err, kErrWaitFree);  // step 1 done
       gather(5, 7);  // G7
       cp_async_wait<3>();
-      publish(&ctl.res_full[2]);
+      publish_slot(&ctl.res_full[2], 2);
       cp_async_wait<2>();
-      publish(&ctl.res_full[3]);
+      publish_slot(&ctl.res_full[3], 3);
       cp_async_wait<1>();
-      publish(&ctl.kst_full[0]);  // slab 5
+      publish_slot(&ctl.kst_full[0], 4);  // slab 5
       if (ok) ok = mbar_wait(&ctl.kst_empty[0], 1, p.err, kErrWaitFree);  // step 4 done
       gather(4, 6);  // G8
       cp_async_wait<1>();
-      publish(&ctl.kst_full[1]);  // slab 7
+      publish_slot(&ctl.kst_full[1], 5);  // slab 7
       cp_async_wait<0>();
-      publish(&ctl.kst_full[0]);  // slab 6
+      publish_slot(&ctl.kst_full[0], 4);  // slab 6
     } else if (tid == 0) {
       // ---- S = Q K^T, nine slab steps -------------------------------------
       const uint32_t idesc = idesc_bf16(128, npad, false);
@@ -482,9 +576,31 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const uint16_t
     // ---- softmax: thread (row, part) takes key columns [128 part, +128) ----
     const float sink2 = (MODE != SA_SINK_NONE && row_valid) ? __ldg(p.sinks + h) * kLog2e : 0.f;
     ok = mbar_wait(&ctl.s_full, 0, p.err, kErrWaitMma) && ok;
+    // fp8 cache: the row scales, after the reductions in the Q staging area
+    // (free once S is complete)
+    float* s_ks = reinterpret_cast<float*>(s_qst + kScaleOffset);
+    if (FP8) {
+      if (warp >= 4) {
+        s_ks[gt] = ks0;
+        s_ks[gt + 128] = ks1;
+      }
+      __syncthreads();
+    }
     __syncwarp();
     tc_fence_after();
     const float c2 = p.scale_log2;
+    // fp8 cache: S holds q . e_r for the unscaled row e_r; the logit is
+    // (q . e_r) s_r.  ks = the row scales of this thread's 32 keys.
+    auto load_scales = [&](int c0, float* ks) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float4 t = *reinterpret_cast<const float4*>(&s_ks[c0 + e]);
+        ks[e] = t.x;
+        ks[e + 1] = t.y;
+        ks[e + 2] = t.z;
+        ks[e + 3] = t.w;
+      }
+    };
     const int k0 = part * 128;
     const int nch = (min(max(npad - k0, 0), 128) + 31) >> 5;
     {
@@ -496,6 +612,12 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const uint16_t
         tmem_ld32(lane_base + kColS + k0 + 32 * ch, v);
         tmem_wait_ld();
         const int c0 = k0 + 32 * ch;
+        if (FP8) {
+          float ks[32];
+          load_scales(c0, ks);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] *= ks[e];
+        }
         if (c0 + 32 > n) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = (c0 + e < n) ? v[e] : -INFINITY;
@@ -525,6 +647,12 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const uint16_t
         tmem_ld32(lane_base + kColS + k0 + 32 * ch, v);
         tmem_wait_ld();
         const int c0 = k0 + 32 * ch;
+        float ks[32];
+        if (FP8) {
+          load_scales(c0, ks);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] *= ks[e];
+        }
         if (c0 + 32 > n) {  // 2^(-inf) = 0 for keys past n
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = (c0 + e < n) ? v[e] : -INFINITY;
@@ -535,7 +663,8 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const uint16_t
           const uint64_t t = f2_fma(f2_pack(v[e], v[e + 1]), c2c2, nmnm);
           const float x0 = ex2_approx(f2_lo(t)), x1 = ex2_approx(f2_hi(t));
           lp[(e >> 1) & 3] = f2_add(lp[(e >> 1) & 3], f2_pack(x0, x1));
-          pk[e >> 1] = pack_bf16x2(x0, x1);
+          // fp8 cache: P V takes the unscaled rows, so P carries s_r
+          pk[e >> 1] = FP8 ? pack_bf16x2(x0 * ks[e], x1 * ks[e + 1]) : pack_bf16x2(x0, x1);
         }
         tmem_st16(lane_base + kColS + k0 + 16 * ch, pk);
       }
@@ -610,12 +739,21 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const uint16_t
       // slabs 4, 5 over R2, R3 (the first P V has read them), landing while
       // the first half is stored
       if (ok) {
-        gather_slab(slot_u32(2), kv, ctl.kidx, iters, n, gr0, gc, 4);
-        gather_slab(slot_u32(3), kv, ctl.kidx, iters, n, gr0, gc, 5);
+        if (FP8) {
+          stage_slab_fp8(slot_u32(2), kv8, ctl.kidx, iters, n, gr0, gc, 4);
+          stage_slab_fp8(slot_u32(3), kv8, ctl.kidx, iters, n, gr0, gc, 5);
+        } else {
+          gather_slab(slot_u32(2), kv, ctl.kidx, iters, n, gr0, gc, 4);
+          gather_slab(slot_u32(3), kv, ctl.kidx, iters, n, gr0, gc, 5);
+        }
       }
       cp_async_commit();
       epilogue(0);
       cp_async_wait<0>();
+      if (FP8) {
+        convert_slab_fp8(slot_u32(2), iters, gr0, gc);
+        convert_slab_fp8(slot_u32(3), iters, gr0, gc);
+      }
       fence_proxy_async();
       mbar_arrive(&ctl.res2_full);
     } else {
@@ -985,9 +1123,9 @@ WorkspaceLayout workspace_layout(int32_t nq, int32_t hq, int32_t topk) {
   return w;
 }
 
-template <int MODE>
+template <int MODE, bool FP8>
 sa_status launch_typed(const IndexArgs& a) {
-  const char* fn = "sa_sparse_index_fwd";
+  const char* fn = a.fn;
   const int nslices = (a.topk + kItemKeys - 1) / kItemKeys;
   uint8_t* ws = reinterpret_cast<uint8_t*>(a.workspace);
   const WorkspaceLayout wl = workspace_layout(a.num_queries, a.num_q_heads, a.topk);
@@ -1015,6 +1153,7 @@ sa_status launch_typed(const IndexArgs& a) {
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return SA_ERR_INVALID_ARG;
   IndexParams p;
+  p.kv_scale = a.kv_scale;
   p.cidx = pp.cidx;
   p.qcount = pp.qcount;
   p.topk = a.topk;
@@ -1033,13 +1172,12 @@ sa_status launch_typed(const IndexArgs& a) {
   p.err = device_error_word();
 
   const size_t smem = 1024 + (size_t)kNumSlots * kSlotBytes + 2 * (size_t)kSlabBytesQ;
-  auto kern = sparse_index_fwd_kernel<MODE>;
+  auto kern = sparse_index_fwd_kernel<MODE, FP8>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   // at most one item per (query, 256 index slots)
   const unsigned items = (unsigned)((int64_t)a.num_queries * nslices * p.nhb);
-  e = launch_dependent(kern, dim3(items), dim3(kThreads), smem, a.stream, tq,
-                       reinterpret_cast<const uint16_t*>(a.kv), p);
+  e = launch_dependent(kern, dim3(items), dim3(kThreads), smem, a.stream, tq, a.kv, p);
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));
   if (nslices > 1) {
     // queries with 2..8 items: TMA-fed combine over the partials viewed as
@@ -1102,10 +1240,14 @@ int sparse_index_max_topk() { return kMaxSlices * kItemKeys; }
 
 sa_status launch_sparse_index_fwd(const IndexArgs& a) {
   if (a.dqk != kDqk || a.dv != kDv)
-    return fail(SA_ERR_UNSUPPORTED,
-                "sa_sparse_index_fwd: dqk %d / dv %d (supported: 576 / 512)", a.dqk, a.dv);
-  if (a.sink_mode == SA_SINK_NULL_LOGIT) return launch_typed<SA_SINK_NULL_LOGIT>(a);
-  return launch_typed<SA_SINK_NONE>(a);
+    return fail(SA_ERR_UNSUPPORTED, "%s: dqk %d / dv %d (supported: 576 / 512)", a.fn, a.dqk,
+                a.dv);
+  if (a.fp8) {
+    if (a.sink_mode == SA_SINK_NULL_LOGIT) return launch_typed<SA_SINK_NULL_LOGIT, true>(a);
+    return launch_typed<SA_SINK_NONE, true>(a);
+  }
+  if (a.sink_mode == SA_SINK_NULL_LOGIT) return launch_typed<SA_SINK_NULL_LOGIT, false>(a);
+  return launch_typed<SA_SINK_NONE, false>(a);
 }
 
 }  // namespace sa

@@ -414,6 +414,10 @@ class IndexFp8Case:
         return int(self.kv.shape[0])
 
     @property
+    def dqk(self) -> int:
+        return int(self.q.shape[2])
+
+    @property
     def topk(self) -> int:
         return int(self.indices.shape[1])
 

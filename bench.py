@@ -255,6 +255,93 @@ class IndexRunner:
                                    c.scale, rows=rows)
 
 
+class IndexFp8Runner(IndexRunner):
+    """sa_sparse_index_fwd_fp8 on the sparse MLA decode workload over an e4m3
+    latent cache with one fp32 scale per row."""
+    oracle_kind = "fp64 numpy oracle (one query per step)"
+
+    @staticmethod
+    def oracle_cores():
+        try:
+            import threadpoolctl
+            n = [i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()
+                 if i.get("user_api") == "blas"]
+            if n:
+                return int(max(n))
+        except ImportError:
+            pass
+        return os.cpu_count() or 1
+
+    def __init__(self, name):
+        self.name = name
+        self.c = W.mla_sparse_decode_fp8(W.SINK_NULL_LOGIT)
+        self.mode = self.c.mode
+
+    def counts(self):
+        """Bytes: q and o once, each listed (valid) e4m3 latent row and its
+        fp32 scale once per query, the index list and the LSE.  Flops as the
+        bf16 cache."""
+        c = self.c
+        nq, hq, dqk = c.q.shape
+        valid = int(((c.indices >= 0) & (c.indices < c.num_kv)).sum())
+        nbytes = (nq * hq * dqk * 2 + nq * hq * c.dv * 2 + valid * (dqk + 4)
+                  + c.indices.nbytes + hq * nq * 4)
+        return nbytes, valid * hq * (2 * dqk + 2 * c.dv)
+
+    def config(self):
+        cfg = super().config()
+        cfg["kv_cache"] = "e4m3 codes + fp32 scale per row"
+        return cfg
+
+    def setup(self, nsets):
+        import torch
+        import attention_head_sinks_gb300 as sa
+        c = self.c
+        dev = torch.device("cuda")
+        self.sets = []
+        for _ in range(nsets):
+            q = _torch_bits(c.q).to(dev)
+            kv = torch.from_numpy(c.kv).to(dev)
+            ks = torch.from_numpy(c.kv_scale).to(dev)
+            idx = torch.from_numpy(c.indices).to(dev)
+            out = torch.empty((c.num_queries, c.num_q_heads, c.dv),
+                              dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((c.num_q_heads, c.num_queries), dtype=torch.float32,
+                              device=dev)
+            self.sets.append((q, kv, ks, idx, out, lse))
+        self.sinks = torch.from_numpy(c.sinks).to(dev)
+        self.ws = torch.empty(max(1, sa.sa_sparse_index_workspace_size(
+            c.num_queries, c.num_q_heads, c.dv, c.topk)), dtype=torch.uint8, device=dev)
+
+    def call(self, i, mode=None):
+        import attention_head_sinks_gb300 as sa
+        q, kv, ks, idx, out, lse = self.sets[i % len(self.sets)]
+        c = self.c
+        sa.sa_sparse_index_fwd_fp8(q, kv, ks, idx, c.dv, self.sinks,
+                                   self.mode if mode is None else mode, c.scale,
+                                   out=out, lse=lse, workspace=self.ws)
+
+    def host_io(self):
+        import torch
+        c = self.c
+        host_in = [_torch_bits(c.q), torch.from_numpy(c.kv), torch.from_numpy(c.kv_scale),
+                   torch.from_numpy(c.indices), torch.from_numpy(c.sinks)]
+        out, lse = self.sets[0][4], self.sets[0][5]
+
+        def run(dev_in):
+            import attention_head_sinks_gb300 as sa
+            sa.sa_sparse_index_fwd_fp8(dev_in[0], dev_in[1], dev_in[2], dev_in[3], c.dv,
+                                       dev_in[4], self.mode, c.scale, out=out, lse=lse,
+                                       workspace=self.ws)
+        return host_in, [out, lse], run
+
+    def oracle(self, rows):
+        from oracle import sa_oracle
+        c = self.c
+        sa_oracle.sparse_index_fwd_fp8(c.q, c.kv, c.kv_scale, c.indices, c.dv, c.sinks,
+                                       self.mode, c.scale, rows=rows)
+
+
 class BlockRunner:
     """sa_block_sparse_fwd on the DSA-style block-sparse prefill."""
     bound = "tensor"
@@ -430,6 +517,7 @@ RUNNERS = {
     "vision_window_4096tok": WindowRunner,
     "gqa_window_16384tok": WindowRunner,
     "mla_sparse_decode": IndexRunner,
+    "mla_sparse_decode_fp8": IndexFp8Runner,
     "dsa_block_prefill": BlockRunner,
     "merge_window_16384tok": MergeRunner,
 }

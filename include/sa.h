@@ -136,7 +136,33 @@ SA_API sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent,
                                      void* workspace, size_t workspace_bytes,
                                      void* stream);
 
-/* Workspace bytes sa_sparse_index_fwd needs for these sizes (0 if none). */
+/*
+ * sa_sparse_index_fwd over an fp8 latent cache -- the decode call site of
+ * afierka-intel/vllm pull 76 ("What": the V4 decode path, whose cache is
+ * fp8).  The page does not fix the cache format; this call takes e4m3 codes
+ * (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 is
+ * subnormal; codes 0x7F / 0xFF are NaN) with one fp32 scale per latent row:
+ * row r's value in column c is e4m3(kv_fp8[r, c]) * kv_scale[r].  K is the
+ * whole row, V its first dv columns, exactly as in sa_sparse_index_fwd; key
+ * sets, sink modes, results, workspace (same size function) and errors are
+ * those of sa_sparse_index_fwd.  The rows enter the MMAs unscaled and exact
+ * (every e4m3 value is a bf16 value); the scale multiplies each logit and
+ * each probability in fp32.
+ *
+ *   kv_fp8     e4m3 bytes [num_kv, dqk], 16-byte aligned
+ *   kv_scale   fp32 [num_kv] (device memory, finite and > 0 for listed rows)
+ */
+SA_API sa_status sa_sparse_index_fwd_fp8(const void* q, const void* kv_fp8,
+                                         const float* kv_scale, int64_t num_kv,
+                                         int32_t dqk, int32_t dv,
+                                         const int32_t* indices, int32_t topk,
+                                         int32_t num_queries, int32_t num_q_heads,
+                                         const float* sinks, int32_t sink_mode,
+                                         float softmax_scale, void* out, float* lse,
+                                         void* workspace, size_t workspace_bytes,
+                                         void* stream);
+
+/* Workspace bytes sa_sparse_index_fwd (and _fp8) needs for these sizes (0 if none). */
 SA_API size_t sa_sparse_index_workspace_size(int32_t num_queries,
                                              int32_t num_q_heads, int32_t dv,
                                              int32_t topk);

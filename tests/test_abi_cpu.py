@@ -115,6 +115,35 @@ def test_sparse_index_rejects_bad_arguments(lib, kw, status, needle):
     assert needle in lib.sa_last_error().decode()
 
 
+def _fp8_call(lib, **kw):
+    a = dict(q=16, kv=16, ks=16, nkv=1000, dqk=576, dv=512, idx=16, topk=2048, nq=64,
+             hq=128, sinks=16, mode=2, scale=0.04, out=16, lse=16, ws=16,
+             ws_bytes=1 << 40)
+    a.update(kw)
+    return lib.sa_sparse_index_fwd_fp8(
+        a["q"], a["kv"], a["ks"], a["nkv"], a["dqk"], a["dv"], a["idx"], a["topk"],
+        a["nq"], a["hq"], a["sinks"], a["mode"], a["scale"], a["out"], a["lse"], a["ws"],
+        a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(ks=None), 1, "NULL"),
+    (dict(ks=18), 1, "misaligned"),
+    (dict(kv=8), 1, "misaligned"),
+    (dict(mode=1), 2, "KEY0_BIAS"),
+    (dict(topk=9000), 2, "topk"),
+    (dict(ws_bytes=1000), 4, "workspace"),
+])
+def test_sparse_index_fp8_rejects_bad_arguments(lib, kw, status, needle):
+    assert _fp8_call(lib, **kw) == status
+    msg = lib.sa_last_error().decode()
+    assert needle in msg and msg.startswith("sa_sparse_index_fwd_fp8")
+
+
+def test_sparse_index_fp8_empty_batch_is_a_no_op(lib):
+    assert _fp8_call(lib, nq=0) == 0
+
+
 def _a256(x):
     return (x + 255) // 256 * 256
 
