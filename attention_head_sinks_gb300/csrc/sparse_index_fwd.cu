@@ -137,9 +137,10 @@ struct IndexRed {
   float m[2][128];
   float l[2][128];
 };
-// fp8 cache: the item's 256 row scales follow the reductions
+// fp8 cache: the item's 256 row scales s_r, then s_r * scale * log2(e),
+// follow the reductions
 constexpr int kScaleOffset = (int)sizeof(IndexRed);
-static_assert(kScaleOffset % 16 == 0 && kScaleOffset + kItemKeys * 4 <= kSlabBytesQ, "");
+static_assert(kScaleOffset % 16 == 0 && kScaleOffset + 2 * kItemKeys * 4 <= kSlabBytesQ, "");
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -303,73 +304,76 @@ __device__ void find_item(const IndexParams& p, int item, IndexSmemCtl& ctl) {
   __syncthreads();
 }
 
-// fp8 cache: 8-byte asynchronous copy (zero-filled when src_bytes is 0).
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
+// fp8 cache: e4m3 bytes (b_lo, b_hi) of word w, picked by `sel`, as a bf16
+// pair.  prmt puts each byte over its sign byte; shifted left by 4 and masked,
+// that is the bf16 encoding of value * 2^-120 (sign, 4 exponent bits, 3
+// mantissa bits; e4m3 subnormals and zero land on bf16 subnormals and zero),
+// and the bf16 multiply by 2^120 gives the value exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w, uint32_t sel) {
+  uint32_t x;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(w), "r"(sel));
+  x = (x << 4) & 0x87f087f0u;
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(0x7B807B80u));  // 2^120
+  return r;
 }
 
-// Eight e4m3 values (byte i = column i) as bf16 pairs.  Every e4m3 value is a
-// bf16 value, and e4m3 -> f16 -> f32 -> bf16 is exact at each step.
-__device__ __forceinline__ uint4 e4m3x8_to_bf16(uint2 raw) {
-  uint32_t h[4];
-  asm("{\n\t.reg .b16 a0, a1, a2, a3;\n\t"
-      "mov.b32 {a0, a1}, %4;\n\t"
-      "mov.b32 {a2, a3}, %5;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, a0;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %1, a1;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %2, a2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %3, a3;\n\t}"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-      : "r"(raw.x), "r"(raw.y));
-  uint32_t o[4];
+// fp8 cache, stage 1: the 64 e4m3 columns of slab `slab` of rows r0 + 32 k
+// (< npad) go, 16 bytes per (row, chunk c4), into the upper half of the 32 KB
+// slot at dst (row r at dst + 16 KB + 64 r); rows past n are zero-filled.
+__device__ __noinline__ void stage_slab_fp8(uint32_t dst, const uint8_t* kv8,
+                                               const int32_t* kidx, int npad, int n, int r0,
+                                               int c4, int slab) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
-    o[i] = pack_bf16x2(f.x, f.y);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// fp8 cache, stage 1: the 64 e4m3 columns of slab `slab` of the slice's rows
-// go, 8 bytes per (row, chunk c), into the upper half of the 32 KB slot at
-// dst (row r at dst + 16 KB + 64 r); rows past n are zero-filled.
-__device__ __forceinline__ void stage_slab_fp8(uint32_t dst, const uint8_t* kv8,
-                                               const int32_t* kidx, int iters, int n, int r0,
-                                               int c, int slab) {
-#pragma unroll 4
-  for (int k = 0; k < iters; ++k) {
-    const int r = r0 + 16 * k;
-    const bool live = r < n;
-    const uint8_t* src = kv8 + (live ? (int64_t)kidx[r] * kDqk + slab * kSlab + c * 8 : 0);
-    cp_async8(dst + kItemKeys * 64 + r * 64 + c * 8, src, live ? 8u : 0u);
+  for (int k = 0; k < kItemKeys / 32; ++k) {
+    const int r = r0 + 32 * k;
+    if (r < npad) {
+      const bool live = r < n;
+      const uint8_t* src = kv8 + (live ? (int64_t)kidx[r] * kDqk + slab * kSlab + c4 * 16 : 0);
+      cp_async16(dst + kItemKeys * 64 + r * 64 + c4 * 16, src, live ? 16u : 0u);
+    }
   }
 }
 
 // fp8 cache, stage 2 (after the staged copies landed): read this thread's
 // staged chunks, wait for every gatherer (bf16 rows 128.. overwrite the
-// staging half), then write the values as bf16 into the slot's
-// 128-byte-swizzled [npad][64] layout.  The row scales are not applied here:
-// the softmax multiplies them into the logits and into P.
-__device__ __forceinline__ void convert_slab_fp8(uint32_t dst, int iters, int r0, int c) {
-  uint2 raw[16];
+// staging half), then write the values as bf16 chunks 2 c4 and 2 c4 + 1 of
+// each row of the slot's 128-byte-swizzled [npad][64] layout.  The row scales
+// are not applied here: the softmax multiplies them into the logits and P.
+// Not inlined (nor the stage above): one copy of the code serves the eleven
+// call sites, each run once per CTA, so it stays in the instruction cache.
+__device__ __noinline__ void convert_slab_fp8(uint32_t dst, int npad, int r0, int c4) {
+  uint4 raw[kItemKeys / 32];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    if (k < iters) {
-      const uint32_t a = dst + kItemKeys * 64 + (r0 + 16 * k) * 64 + c * 8;
-      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(raw[k].x), "=r"(raw[k].y) : "r"(a));
+  for (int k = 0; k < kItemKeys / 32; ++k) {
+    const int r = r0 + 32 * k;
+    if (r < npad) {
+      const uint32_t a = dst + kItemKeys * 64 + r * 64 + c4 * 16;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(raw[k].x), "=r"(raw[k].y), "=r"(raw[k].z), "=r"(raw[k].w)
+                   : "r"(a));
     }
   }
   bar_gather();
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    if (k < iters) {
-      const int r = r0 + 16 * k;
-      const uint4 v = e4m3x8_to_bf16(raw[k]);
-      const uint32_t a = dst + r * 128 + ((c ^ (r & 7)) << 4);
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
-                   "r"(v.z), "r"(v.w)
+  for (int k = 0; k < kItemKeys / 32; ++k) {
+    const int r = r0 + 32 * k;
+    if (r < npad) {
+      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        o[2 * i] = e4m3x2_to_bf16x2(w[i], 0x9180u);      // bytes 0, 1
+        o[2 * i + 1] = e4m3x2_to_bf16x2(w[i], 0xB3A2u);  // bytes 2, 3
+      }
+      const uint32_t row = dst + r * 128;
+      const uint32_t a0 = row + (((2 * c4) ^ (r & 7)) << 4);
+      const uint32_t a1 = row + (((2 * c4 + 1) ^ (r & 7)) << 4);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(o[0]), "r"(o[1]),
+                   "r"(o[2]), "r"(o[3])
+                   : "memory");
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(o[4]), "r"(o[5]),
+                   "r"(o[6]), "r"(o[7])
                    : "memory");
     }
   }
@@ -451,6 +455,7 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
     // gr0 + 16 k of every slab
     const int gt = tid - 128;
     const int gr0 = (gt >> 3) & 15, gc = gt & 7;
+    const int fr0 = gt >> 2, fc4 = gt & 3;  // fp8 cache: rows fr0 + 32 k, 16-byte chunk fc4
     const int iters = npad >> 4;
     float ks0 = 0.f, ks1 = 0.f;
     if (warp >= 4) {
@@ -469,14 +474,14 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
     if (warp >= 4) {
       auto gather = [&](int slot, int slab) {
         if (ok) {
-          if (FP8) stage_slab_fp8(slot_u32(slot), kv8, ctl.kidx, iters, n, gr0, gc, slab);
+          if (FP8) stage_slab_fp8(slot_u32(slot), kv8, ctl.kidx, npad, n, fr0, fc4, slab);
           else gather_slab(slot_u32(slot), kv, ctl.kidx, iters, n, gr0, gc, slab);
         }
         cp_async_commit();
       };
       // the slot's copies have landed: (fp8: convert it, then) hand it over
       auto publish_slot = [&](uint64_t* bar, int slot) {
-        if (FP8) convert_slab_fp8(slot_u32(slot), iters, gr0, gc);
+        if (FP8) convert_slab_fp8(slot_u32(slot), npad, fr0, fc4);
         fence_proxy_async();
         mbar_arrive(bar);
       };
@@ -490,9 +495,10 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
       // DRAM reads now so that the copies find them in L2
       for (int r = gt; r < n; r += 128) {
         const int64_t row = (int64_t)ctl.kidx[r] * kDqk;
-        if (FP8) {
+        if (FP8) {  // bytes [320, 512): every 128-byte line holds one of these
           prefetch_l2(kv8 + row + 5 * kSlab);
           prefetch_l2(kv8 + row + 7 * kSlab);
+          prefetch_l2(kv8 + row + 8 * kSlab - 1);
         } else {
           prefetch_l2(kv + row + 5 * kSlab);
           prefetch_l2(kv + row + 6 * kSlab);
@@ -579,26 +585,31 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
     // fp8 cache: the row scales, after the reductions in the Q staging area
     // (free once S is complete)
     float* s_ks = reinterpret_cast<float*>(s_qst + kScaleOffset);
+    float* s_kc = s_ks + kItemKeys;
     if (FP8) {
       if (warp >= 4) {
+        // keys past n: scale 0 (P = 0) and logit factor 1 (their -inf mask
+        // must not meet a zero factor)
         s_ks[gt] = ks0;
         s_ks[gt + 128] = ks1;
+        s_kc[gt] = gt < n ? ks0 * p.scale_log2 : 1.f;
+        s_kc[gt + 128] = gt + 128 < n ? ks1 * p.scale_log2 : 1.f;
       }
       __syncthreads();
     }
     __syncwarp();
     tc_fence_after();
     const float c2 = p.scale_log2;
-    // fp8 cache: S holds q . e_r for the unscaled row e_r; the logit is
-    // (q . e_r) s_r.  ks = the row scales of this thread's 32 keys.
-    auto load_scales = [&](int c0, float* ks) {
+    // fp8 cache: S holds q . e_r for the unscaled row e_r; the log2-domain
+    // logit is (q . e_r) * kc_r with kc_r = s_r * scale * log2(e).
+    auto load32 = [&](const float* src, float* dst) {
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
-        const float4 t = *reinterpret_cast<const float4*>(&s_ks[c0 + e]);
-        ks[e] = t.x;
-        ks[e + 1] = t.y;
-        ks[e + 2] = t.z;
-        ks[e + 3] = t.w;
+        const float4 t = *reinterpret_cast<const float4*>(src + e);
+        dst[e] = t.x;
+        dst[e + 1] = t.y;
+        dst[e + 2] = t.z;
+        dst[e + 3] = t.w;
       }
     };
     const int k0 = part * 128;
@@ -613,10 +624,15 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
         tmem_wait_ld();
         const int c0 = k0 + 32 * ch;
         if (FP8) {
-          float ks[32];
-          load_scales(c0, ks);
+          float kc[32];
+          load32(s_kc + c0, kc);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] *= ks[e];
+          for (int e = 0; e < 32; e += 2) {
+            const uint64_t t = f2_fma(f2_pack(v[e], v[e + 1]), f2_pack(kc[e], kc[e + 1]),
+                                      f2_pack(-0.f, -0.f));
+            v[e] = f2_lo(t);
+            v[e + 1] = f2_hi(t);
+          }
         }
         if (c0 + 32 > n) {
 #pragma unroll
@@ -633,8 +649,9 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
       red.m[part][row] = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
     }
     __syncthreads();
-    // max(s) * c2 == max(s * c2) exactly (c2 > 0, rounding is monotone)
-    const float m = fmaxf(red.m[0][row], red.m[1][row]) * c2;
+    // max(s) * c2 == max(s * c2) exactly (c2 > 0, rounding is monotone); the
+    // fp8 maxima are already in the log2 domain
+    const float m = fmaxf(red.m[0][row], red.m[1][row]) * (FP8 ? 1.f : c2);
     {
       // pass 2: P = 2^(s c2 - m) (bf16, written over S: key columns [k0, k0 +
       // 128) go to TMEM columns [k0, k0 + 64), inside this thread's half) and
@@ -647,11 +664,10 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
         tmem_ld32(lane_base + kColS + k0 + 32 * ch, v);
         tmem_wait_ld();
         const int c0 = k0 + 32 * ch;
-        float ks[32];
+        float ks[32], kc[32];
         if (FP8) {
-          load_scales(c0, ks);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] *= ks[e];
+          load32(s_kc + c0, kc);
+          load32(s_ks + c0, ks);
         }
         if (c0 + 32 > n) {  // 2^(-inf) = 0 for keys past n
 #pragma unroll
@@ -660,11 +676,18 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const uint64_t t = f2_fma(f2_pack(v[e], v[e + 1]), c2c2, nmnm);
+          const uint64_t t = f2_fma(f2_pack(v[e], v[e + 1]),
+                                    FP8 ? f2_pack(kc[e], kc[e + 1]) : c2c2, nmnm);
           const float x0 = ex2_approx(f2_lo(t)), x1 = ex2_approx(f2_hi(t));
           lp[(e >> 1) & 3] = f2_add(lp[(e >> 1) & 3], f2_pack(x0, x1));
           // fp8 cache: P V takes the unscaled rows, so P carries s_r
-          pk[e >> 1] = FP8 ? pack_bf16x2(x0 * ks[e], x1 * ks[e + 1]) : pack_bf16x2(x0, x1);
+          if (FP8) {
+            const uint64_t w = f2_fma(f2_pack(x0, x1), f2_pack(ks[e], ks[e + 1]),
+                                      f2_pack(-0.f, -0.f));
+            pk[e >> 1] = pack_bf16x2(f2_lo(w), f2_hi(w));
+          } else {
+            pk[e >> 1] = pack_bf16x2(x0, x1);
+          }
         }
         tmem_st16(lane_base + kColS + k0 + 16 * ch, pk);
       }
@@ -740,8 +763,8 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
       // the first half is stored
       if (ok) {
         if (FP8) {
-          stage_slab_fp8(slot_u32(2), kv8, ctl.kidx, iters, n, gr0, gc, 4);
-          stage_slab_fp8(slot_u32(3), kv8, ctl.kidx, iters, n, gr0, gc, 5);
+          stage_slab_fp8(slot_u32(2), kv8, ctl.kidx, npad, n, fr0, fc4, 4);
+          stage_slab_fp8(slot_u32(3), kv8, ctl.kidx, npad, n, fr0, fc4, 5);
         } else {
           gather_slab(slot_u32(2), kv, ctl.kidx, iters, n, gr0, gc, 4);
           gather_slab(slot_u32(3), kv, ctl.kidx, iters, n, gr0, gc, 5);
@@ -751,8 +774,8 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
       epilogue(0);
       cp_async_wait<0>();
       if (FP8) {
-        convert_slab_fp8(slot_u32(2), iters, gr0, gc);
-        convert_slab_fp8(slot_u32(3), iters, gr0, gc);
+        convert_slab_fp8(slot_u32(2), npad, fr0, fc4);
+        convert_slab_fp8(slot_u32(3), npad, fr0, fc4);
       }
       fence_proxy_async();
       mbar_arrive(&ctl.res2_full);
