@@ -331,6 +331,43 @@ def dsa_block_prefill(mode=SINK_NULL_LOGIT, seed=1005, pad_rows=0,
 
 
 # --------------------------------------------------------------------------
+# indexer inputs for on-device block selection
+# --------------------------------------------------------------------------
+@dataclasses.dataclass
+class SelectCase:
+    name: str
+    index_q: np.ndarray   # uint16 bf16 [B*S, Hi, Di]
+    index_k: np.ndarray   # uint16 bf16 [B*S, Di]
+    batch: int
+    seq_len: int
+    block_size: int
+    topk: int
+
+    @property
+    def num_index_heads(self) -> int:
+        return int(self.index_q.shape[1])
+
+    @property
+    def index_dim(self) -> int:
+        return int(self.index_q.shape[2])
+
+
+def select_case(batch, seq_len, hi, di, block_size, topk, seed,
+                name="block_select") -> SelectCase:
+    """Index queries [B*S, Hi, Di] and index keys [B*S, Di] ~ N(0,1) bf16."""
+    rng = _rng(seed)
+    T = batch * seq_len
+    return SelectCase(name, bf16_normal(rng, (T, hi, di)), bf16_normal(rng, (T, di)),
+                      batch, seq_len, block_size, topk)
+
+
+def dsa_block_select(seed=1008) -> SelectCase:
+    """Indexer inputs of the DSA prefill batch: 2 x 8192 tokens, 4 index
+    heads of dim 128, key block 64, top-16 blocks per (index head, token)."""
+    return select_case(2, 8192, 4, 128, 64, 16, seed, "dsa_block_select_2x8192")
+
+
+# --------------------------------------------------------------------------
 # two partial attention results to merge (cascade over two key sets)
 # --------------------------------------------------------------------------
 @dataclasses.dataclass

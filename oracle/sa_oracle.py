@@ -228,3 +228,85 @@ def sparse_index_fwd_fp8(q, kv, kv_scale, indices, dv, sinks, mode, scale, rows=
             den = den + np.exp(sk)[:, None]
         out[i] = (np.exp(logits) @ rows_f[:, :dv]) / den
     return out, lse, cnt
+
+
+def block_select(index_q, index_k, batch, seq_len, block_size, topk, rows=None):
+    """Top-k key blocks per (index head, query token) from indexer scores
+    ([M3 CP sparse] forward step 3 and ``_select_local_blocks``: the selection
+    is built from index q / k over the causal sequence of the token's batch
+    row, one selection per index head; documents are not consulted -- their
+    mask is applied inside the attention).  Readings where the page is
+    silent: the token score is the dot product q_idx[i, g] . k_idx[j]; a
+    block's score is the max over its causal keys; the query's own (diagonal)
+    block is always selected and the other ``topk - 1`` are the highest
+    scoring earlier blocks, ties to the lower block id; a token with at most
+    ``topk`` causal blocks selects them all.
+
+    index_q ``[B*S, Hi, Di]`` and index_k ``[B*S, Di]`` (bf16 bits as uint16,
+    or float).  Scores in fp64 from the exact inputs.  Returns the table
+    ``[Hi, B*S, topk]`` int32 (ascending block ids, -1 padded) and the block
+    scores ``[Hi, B*S, nblocks]`` float64 (-inf for blocks at or after the
+    diagonal).  ``rows=(begin, end)`` restricts the work to those tokens (the
+    rest of the table is -2, of the scores NaN).
+    """
+    qf = _widen(index_q)
+    kf = _widen(index_k)
+    T, hi, di = qf.shape
+    nb = -(-seq_len // block_size)
+    b0, e0 = (0, T) if rows is None else rows
+    table = np.full((hi, T, topk), -2, np.int32)
+    scores = np.full((hi, T, nb), np.nan)
+    table[:, b0:e0] = -1
+    for i in range(b0, e0):
+        row0 = (i // seq_len) * seq_len
+        pos = i - row0
+        diag = pos // block_size
+        keys = kf[row0:row0 + diag * block_size]          # keys of earlier blocks
+        tok = qf[i] @ keys.T                              # [hi, diag * block_size]
+        blk = tok.reshape(hi, diag, block_size).max(axis=2) if diag else \
+            np.zeros((hi, 0))
+        scores[:, i, :] = -np.inf
+        scores[:, i, :diag] = blk
+        for g in range(hi):
+            if diag + 1 <= topk:
+                sel = np.arange(diag + 1)
+            else:
+                # highest score first; among equal scores the lower id first
+                order = np.lexsort((np.arange(diag), -blk[g]))[:topk - 1]
+                sel = np.sort(np.append(order, diag))
+            table[g, i, :len(sel)] = sel
+    return table, scores
+
+
+def block_sparse_fwd_index_heads(q, k, v, batch, seq_len, tables, block_size, cu_docs,
+                                 sinks, mode, scale, rows=None):
+    """Block-sparse attention with one selection per index head: attention
+    head h uses ``tables[h // (Hq / Hi)]`` ([M3 CP sparse] ``_select_local_blocks``
+    returns ``[batch, index_heads, sequence, key_blocks]``); each group of
+    heads is ``block_sparse_fwd`` with its own table.  tables ``[Hi, B*S,
+    topk]``; Hi must divide Hkv (a KV head's query heads share one index
+    head).  Returns out ``[B*S,Hq,D]``, lse ``[Hq,B*S]``, key counts
+    ``[Hi, B*S]``.
+    """
+    tables = np.asarray(tables, np.int32)
+    hi = tables.shape[0]
+    T, hq, d = np.asarray(q).shape
+    hkv = np.asarray(k).shape[1]
+    if hkv % hi:
+        raise ValueError("the number of index heads must divide the KV heads")
+    gq, gk = hq // hi, hkv // hi
+    s = _sinks(sinks, hq)
+    out = np.full((T, hq, d), np.nan)
+    lse = np.full((hq, T), np.nan)
+    cnt = np.full((hi, T), -1, np.int32)
+    for g in range(hi):
+        o, l, c = block_sparse_fwd(
+            np.ascontiguousarray(np.asarray(q)[:, g * gq:(g + 1) * gq]),
+            np.ascontiguousarray(np.asarray(k)[:, g * gk:(g + 1) * gk]),
+            np.ascontiguousarray(np.asarray(v)[:, g * gk:(g + 1) * gk]),
+            batch, seq_len, tables[g], block_size, cu_docs,
+            s[g * gq:(g + 1) * gq], mode, scale, rows=rows)
+        out[:, g * gq:(g + 1) * gq] = o
+        lse[g * gq:(g + 1) * gq] = l
+        cnt[g] = c
+    return out, lse, cnt
