@@ -12,7 +12,7 @@ from ._lib import SAError, lib  # noqa: F401
 from .workloads import SINK_KEY0_BIAS, SINK_NONE, SINK_NULL_LOGIT  # noqa: F401
 
 __all__ = ["sa_varlen_window_fwd", "sa_sparse_index_fwd", "sa_sparse_index_fwd_fp8",
-           "sa_block_sparse_fwd",
+           "sa_block_sparse_fwd", "sa_block_sparse_fwd_index_heads", "sa_block_select",
            "sa_merge_attn_states",
            "sa_sparse_index_workspace_size", "sa_device_error", "sa_version", "SAError",
            "SINK_NONE", "SINK_KEY0_BIAS", "SINK_NULL_LOGIT"]
@@ -176,6 +176,70 @@ def sa_sparse_index_fwd_fp8(q, kv_fp8, kv_scale, indices, dv, sinks, sink_mode,
         None if sinks is None else sinks.data_ptr(), int(sink_mode),
         float(softmax_scale), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes,
         _stream_handle(stream)))
+    return out, lse
+
+
+def sa_block_select(index_q, index_k, batch, seq_len, block_size, topk_blocks,
+                    block_table=None, stream=None):
+    """Top-k key blocks per (index head, token) from indexer scores (C:
+    ``sa_block_select``).
+
+    index_q ``[B*S,Hi,Di]`` and index_k ``[B*S,Di]`` bf16.  Returns the block
+    table int32 ``[Hi,B*S,topk]`` (ascending, -1 padded).
+    """
+    torch = _torch()
+    _dev_tensor("index_q", index_q, torch.bfloat16, 3)
+    _dev_tensor("index_k", index_k, torch.bfloat16, 2)
+    T, hi, di = index_q.shape
+    if T != batch * seq_len or index_k.shape != (T, di):
+        raise ValueError("index_q must be [batch*seq_len, Hi, Di] and index_k [batch*seq_len, Di]")
+    if block_table is None:
+        block_table = torch.empty((hi, T, int(topk_blocks)), dtype=torch.int32,
+                                  device=index_q.device)
+    _dev_tensor("block_table", block_table, torch.int32, 3)
+    if block_table.shape != (hi, T, int(topk_blocks)):
+        raise ValueError("block_table must be [Hi, batch*seq_len, topk_blocks]")
+    from ._lib import check
+    check(lib().sa_block_select(
+        index_q.data_ptr(), index_k.data_ptr(), int(batch), int(seq_len), hi, di,
+        int(block_size), int(topk_blocks), block_table.data_ptr(), _stream_handle(stream)))
+    return block_table
+
+
+def sa_block_sparse_fwd_index_heads(q, k, v, batch, seq_len, block_table, block_size,
+                                    cu_docs, sinks, sink_mode, softmax_scale, out=None,
+                                    lse=None, stream=None):
+    """Block-sparse attention with one selection per index head (C:
+    ``sa_block_sparse_fwd_index_heads``): block_table int32 ``[Hi,B*S,topk]``;
+    query head h uses table ``h // (Hq / Hi)``.  Otherwise as
+    ``sa_block_sparse_fwd``."""
+    torch = _torch()
+    _dev_tensor("q", q, torch.bfloat16, 3)
+    _dev_tensor("k", k, torch.bfloat16, 3)
+    _dev_tensor("v", v, torch.bfloat16, 3)
+    _dev_tensor("block_table", block_table, torch.int32, 3)
+    _dev_tensor("cu_docs", cu_docs, torch.int32, 1)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    if T != batch * seq_len or k.shape != (T, hkv, d) or v.shape != (T, hkv, d):
+        raise ValueError("q must be [batch*seq_len, Hq, D] and k, v [batch*seq_len, Hkv, D]")
+    if block_table.shape[1] != T:
+        raise ValueError("block_table must be [Hi, batch*seq_len, topk]")
+    if sinks is not None:
+        _dev_tensor("sinks", sinks, torch.float32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    _dev_tensor("out", out, torch.bfloat16, 3)
+    _dev_tensor("lse", lse, torch.float32, 2)
+    from ._lib import check
+    check(lib().sa_block_sparse_fwd_index_heads(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), int(batch), int(seq_len), hq, hkv, d,
+        block_table.data_ptr(), block_table.shape[0], block_table.shape[2],
+        int(block_size), cu_docs.data_ptr(), cu_docs.numel() - 1,
+        None if sinks is None else sinks.data_ptr(), int(sink_mode),
+        float(softmax_scale), out.data_ptr(), lse.data_ptr(), _stream_handle(stream)))
     return out, lse
 
 

@@ -40,6 +40,11 @@ SIGNATURES = {
     "sa_block_sparse_fwd": (ctypes.c_int, [
         _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _I32, _P, _I32, _P,
         _I32, _F32, _P, _P, _P, _SZ, _P]),
+    "sa_block_sparse_fwd_index_heads": (ctypes.c_int, [
+        _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _I32, _I32, _P, _I32,
+        _P, _I32, _F32, _P, _P, _P]),
+    "sa_block_select": (ctypes.c_int, [
+        _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P]),
     "sa_merge_attn_states": (ctypes.c_int, [
         _P, _P, _P, _P, _I64, _I32, _I32, _P, _I32, _P, _P, _P]),
     "sa_last_error": (ctypes.c_char_p, []),

@@ -12,6 +12,9 @@
 // key of the token's document (vLLM pull 49815, second paragraph, with
 // documents as the sequences), when that key is in the token's set.
 //
+// With several index heads (one selection each, [M3 CP sparse]
+// _select_local_blocks), a KV head's query heads share one: KV head g reads
+// the table of index head g / (Hkv / Hi).
 // Tile: M = 128 rows = (128 / G) consecutive tokens x the G query heads of
 // one KV head (row = token * G + head).  Keys: the union, over the tile's
 // tokens, of their selected blocks that intersect [document start, token] --
@@ -53,7 +56,9 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr int kThreads = 384;  // warps 0..3: roles; 4..7 and 8..11: softmax parts 0 and 1
 
 struct BlockParams {
-  const int32_t* table;  // [T, topk]
+  const int32_t* table;  // [Hi, T, topk]
+  int64_t table_head_stride;  // T * topk
+  int32_t kv_per_index_head;  // Hkv / Hi
   int32_t topk;
   int32_t seq_len;
   int32_t nblocks;
@@ -152,6 +157,8 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   // overlap them.
   constexpr int kPairsPerThread = (kMaxUnion + kThreads - 1) / kThreads;
   const int npairs = TQ * p.topk;  // <= kMaxUnion (checked on the host)
+  // the selection of this KV head's index head
+  const int32_t* table = p.table + (int64_t)(g / p.kv_per_index_head) * p.table_head_stride;
   int32_t sel[kPairsPerThread];
 #pragma unroll
   for (int k = 0; k < kPairsPerThread; ++k) {
@@ -160,7 +167,7 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (w < npairs) {
       const int i = w / p.topk;
       if (tok0 + i < p.total_tokens)
-        sel[k] = __ldg(p.table + (int64_t)(tok0 + i) * p.topk + (w - i * p.topk));
+        sel[k] = __ldg(table + (int64_t)(tok0 + i) * p.topk + (w - i * p.topk));
     }
   }
   if (tid < TQ) {
@@ -563,6 +570,8 @@ sa_status launch_typed(const BlockArgs& a) {
     return SA_ERR_INVALID_ARG;
   BlockParams p;
   p.table = a.block_table;
+  p.table_head_stride = T * a.topk_blocks;
+  p.kv_per_index_head = a.num_kv_heads / a.num_index_heads;
   p.topk = a.topk_blocks;
   p.seq_len = a.seq_len;
   p.nblocks = a.seq_len / kBlk;

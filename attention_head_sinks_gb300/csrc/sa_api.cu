@@ -188,16 +188,15 @@ sa_status sa_varlen_window_fwd(const void* q, const void* k, const void* v,
   return sa::launch_window_fwd(a);
 }
 
-sa_status sa_block_sparse_fwd(const void* q, const void* k, const void* v, int32_t batch,
-                              int32_t seq_len, int32_t num_q_heads, int32_t num_kv_heads,
-                              int32_t head_dim, const int32_t* block_table,
-                              int32_t topk_blocks, int32_t block_size,
-                              const int32_t* cu_docs, int32_t num_docs, const float* sinks,
-                              int32_t sink_mode, float softmax_scale, void* out, float* lse,
-                              void* workspace, size_t workspace_bytes, void* stream) {
-  const char* fn = "sa_block_sparse_fwd";
-  (void)workspace;
-  (void)workspace_bytes;
+namespace {
+// Shared checks and dispatch of the single-table and per-index-head entries.
+sa_status block_sparse_entry(const char* fn, const void* q, const void* k, const void* v,
+                             int32_t batch, int32_t seq_len, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim,
+                             const int32_t* block_table, int32_t num_index_heads,
+                             int32_t topk_blocks, int32_t block_size, const int32_t* cu_docs,
+                             int32_t num_docs, const float* sinks, int32_t sink_mode,
+                             float softmax_scale, void* out, float* lse, void* stream) {
   if (!q || !k || !v || !cu_docs || !out || !lse || (topk_blocks > 0 && !block_table))
     return fail(SA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
   if (sink_mode < SA_SINK_NONE || sink_mode > SA_SINK_NULL_LOGIT)
@@ -214,6 +213,10 @@ sa_status sa_block_sparse_fwd(const void* q, const void* k, const void* v, int32
     return fail(SA_ERR_INVALID_ARG,
                 "%s: num_q_heads %d must be a positive multiple of num_kv_heads %d", fn,
                 num_q_heads, num_kv_heads);
+  if (num_index_heads < 1 || num_kv_heads % num_index_heads != 0)
+    return fail(SA_ERR_INVALID_ARG,
+                "%s: num_index_heads %d must divide num_kv_heads %d", fn, num_index_heads,
+                num_kv_heads);
   if ((int64_t)batch * seq_len >= ((int64_t)1 << 31))
     return fail(SA_ERR_INVALID_ARG, "%s: batch * seq_len >= 2^31", fn);
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale))
@@ -235,6 +238,7 @@ sa_status sa_block_sparse_fwd(const void* q, const void* k, const void* v, int32
   a.num_kv_heads = num_kv_heads;
   a.head_dim = head_dim;
   a.block_table = block_table;
+  a.num_index_heads = num_index_heads;
   a.topk_blocks = topk_blocks;
   a.block_size = block_size;
   a.cu_docs = cu_docs;
@@ -246,6 +250,68 @@ sa_status sa_block_sparse_fwd(const void* q, const void* k, const void* v, int32
   a.lse = lse;
   a.stream = static_cast<cudaStream_t>(stream);
   return sa::launch_block_sparse_fwd(a);
+}
+}  // namespace
+
+sa_status sa_block_sparse_fwd(const void* q, const void* k, const void* v, int32_t batch,
+                              int32_t seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, const int32_t* block_table,
+                              int32_t topk_blocks, int32_t block_size,
+                              const int32_t* cu_docs, int32_t num_docs, const float* sinks,
+                              int32_t sink_mode, float softmax_scale, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  return block_sparse_entry("sa_block_sparse_fwd", q, k, v, batch, seq_len, num_q_heads,
+                            num_kv_heads, head_dim, block_table, 1, topk_blocks, block_size,
+                            cu_docs, num_docs, sinks, sink_mode, softmax_scale, out, lse,
+                            stream);
+}
+
+sa_status sa_block_sparse_fwd_index_heads(
+    const void* q, const void* k, const void* v, int32_t batch, int32_t seq_len,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, const int32_t* block_table,
+    int32_t num_index_heads, int32_t topk_blocks, int32_t block_size, const int32_t* cu_docs,
+    int32_t num_docs, const float* sinks, int32_t sink_mode, float softmax_scale, void* out,
+    float* lse, void* stream) {
+  return block_sparse_entry("sa_block_sparse_fwd_index_heads", q, k, v, batch, seq_len,
+                            num_q_heads, num_kv_heads, head_dim, block_table, num_index_heads,
+                            topk_blocks, block_size, cu_docs, num_docs, sinks, sink_mode,
+                            softmax_scale, out, lse, stream);
+}
+
+sa_status sa_block_select(const void* index_q, const void* index_k, int32_t batch,
+                          int32_t seq_len, int32_t num_index_heads, int32_t index_dim,
+                          int32_t block_size, int32_t topk_blocks, int32_t* block_table,
+                          void* stream) {
+  const char* fn = "sa_block_select";
+  if (!index_q || !index_k || !block_table)
+    return fail(SA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (batch < 0 || seq_len < 0 || num_index_heads < 1 || index_dim < 1 || block_size < 1 ||
+      topk_blocks < 1)
+    return fail(SA_ERR_INVALID_ARG,
+                "%s: bad sizes (batch %d, seq_len %d, num_index_heads %d, index_dim %d, "
+                "block_size %d, topk_blocks %d)",
+                fn, batch, seq_len, num_index_heads, index_dim, block_size, topk_blocks);
+  if ((int64_t)batch * seq_len >= ((int64_t)1 << 31))
+    return fail(SA_ERR_INVALID_ARG, "%s: batch * seq_len >= 2^31", fn);
+  if (!sa::aligned(index_q, 16) || !sa::aligned(index_k, 16) || !sa::aligned(block_table, 4))
+    return fail(SA_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  if ((int64_t)batch * seq_len == 0) return SA_OK;
+  if (!sa::device_error_word())
+    return fail(SA_ERR_CUDA, "%s: no usable CUDA device", fn);
+  sa::SelectArgs a;
+  a.index_q = index_q;
+  a.index_k = index_k;
+  a.batch = batch;
+  a.seq_len = seq_len;
+  a.num_index_heads = num_index_heads;
+  a.index_dim = index_dim;
+  a.block_size = block_size;
+  a.topk_blocks = topk_blocks;
+  a.block_table = block_table;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return sa::launch_block_select(a);
 }
 
 size_t sa_sparse_index_workspace_size(int32_t num_queries, int32_t num_q_heads,

@@ -113,7 +113,8 @@ struct BlockArgs {
   int32_t num_q_heads;
   int32_t num_kv_heads;
   int32_t head_dim;
-  const int32_t* block_table;
+  const int32_t* block_table;  // [num_index_heads, T, topk]
+  int32_t num_index_heads;     // divides num_kv_heads
   int32_t topk_blocks;
   int32_t block_size;
   const int32_t* cu_docs;
@@ -127,6 +128,21 @@ struct BlockArgs {
 };
 
 sa_status launch_block_sparse_fwd(const BlockArgs& a);
+
+struct SelectArgs {
+  const void* index_q;  // bf16 [T, Hi, Di]
+  const void* index_k;  // bf16 [T, Di]
+  int32_t batch;
+  int32_t seq_len;
+  int32_t num_index_heads;
+  int32_t index_dim;
+  int32_t block_size;
+  int32_t topk_blocks;
+  int32_t* block_table;  // [Hi, T, topk] (written)
+  cudaStream_t stream;
+};
+
+sa_status launch_block_select(const SelectArgs& a);
 
 struct MergeArgs {
   const void* out_a;

@@ -512,6 +512,170 @@ class MergeRunner:
                                c.sinks, self.mode)
 
 
+class SelectRunner:
+    """sa_block_select on the indexer inputs of the DSA prefill batch."""
+    bound = "tensor"
+    source = "attention_head_sinks_gb300/csrc/block_select.cu"
+    oracle_kind = "fp64 numpy oracle (one token per step)"
+
+    @staticmethod
+    def oracle_cores():
+        return IndexFp8Runner.oracle_cores()
+
+    def __init__(self, name):
+        self.name = name
+        self.c = W.dsa_block_select()
+        self.mode = W.SINK_NONE
+
+    def counts(self):
+        """Bytes: index q, index k and the table once.  Flops: 2 * Di per
+        (token, index head, key of a block before the token's own)."""
+        c = self.c
+        T, hi, di = c.index_q.shape
+        pos = np.arange(T) % c.seq_len
+        keys = int(((pos // c.block_size) * c.block_size).sum())
+        nbytes = c.index_q.nbytes + c.index_k.nbytes + hi * T * c.topk * 4
+        return nbytes, keys * hi * 2 * di
+
+    def config(self):
+        c = self.c
+        return {"workload": self.name, "batch": c.batch, "seq_len": c.seq_len,
+                "index_heads": c.num_index_heads, "index_dim": c.index_dim,
+                "block_size": c.block_size, "topk_blocks": c.topk,
+                "flops_basis": "keys of the blocks each token ranks"}
+
+    def setup(self, nsets):
+        import torch
+        c = self.c
+        dev = torch.device("cuda")
+        T = c.batch * c.seq_len
+        self.sets = []
+        for _ in range(nsets):
+            qi, ki = _torch_bits(c.index_q).to(dev), _torch_bits(c.index_k).to(dev)
+            tab = torch.empty((c.num_index_heads, T, c.topk), dtype=torch.int32, device=dev)
+            self.sets.append((qi, ki, tab))
+
+    def touched_bytes(self):
+        return self.counts()[0]
+
+    def launches_per_call(self):
+        return 1
+
+    def call(self, i, mode=None):
+        import attention_head_sinks_gb300 as sa
+        qi, ki, tab = self.sets[i % len(self.sets)]
+        c = self.c
+        sa.sa_block_select(qi, ki, c.batch, c.seq_len, c.block_size, c.topk, block_table=tab)
+
+    def host_io(self):
+        c = self.c
+        host_in = [_torch_bits(c.index_q), _torch_bits(c.index_k)]
+        tab = self.sets[0][2]
+
+        def run(dev_in):
+            import attention_head_sinks_gb300 as sa
+            sa.sa_block_select(dev_in[0], dev_in[1], c.batch, c.seq_len, c.block_size, c.topk,
+                               block_table=tab)
+        return host_in, [tab], run
+
+    def oracle_rows(self):
+        return self.c.batch * self.c.seq_len
+
+    def oracle(self, rows):
+        from oracle import sa_oracle
+        c = self.c
+        sa_oracle.block_select(c.index_q, c.index_k, c.batch, c.seq_len, c.block_size, c.topk,
+                               rows=rows)
+
+
+class SelectedBlockRunner(BlockRunner):
+    """The DSA prefill step with its selection made on the device:
+    sa_block_select (4 index heads, one per KV head) then
+    sa_block_sparse_fwd_index_heads with those tables."""
+    oracle_kind = "fp64 numpy selection + fp64 C attention oracle with OpenMP"
+
+    def __init__(self, name):
+        super().__init__(name)
+        self.sc = W.dsa_block_select()
+
+    def counts(self):
+        """Bytes: the attention's (q, o, k, v, LSE) plus the indexer inputs
+        and the table.  Flops: the selection's plus the attention's over the
+        selected blocks, which are those of the tables the selection writes
+        (their count is fixed by the shape: every token selects
+        min(own block + 1, topk) blocks)."""
+        c, sc = self.c, self.sc
+        T, hq, d = c.q.shape
+        hkv = c.k.shape[1]
+        pos = np.arange(T) % c.seq_len
+        nsel = np.minimum(pos // c.block_size + 1, sc.topk)
+        hi = sc.num_index_heads
+        att_flops = int(nsel.sum()) * c.block_size * hq * 4 * d
+        keys = int(((pos // sc.block_size) * sc.block_size).sum())
+        sel_flops = keys * hi * 2 * sc.index_dim
+        nbytes = (2 * T * hq * d * 2 + 2 * T * hkv * d * 2 + hq * T * 4 + sc.index_q.nbytes
+                  + sc.index_k.nbytes + 2 * hi * T * sc.topk * 4)
+        return nbytes, att_flops + sel_flops
+
+    def config(self):
+        cfg = super().config()
+        cfg.update({"index_heads": self.sc.num_index_heads, "index_dim": self.sc.index_dim,
+                    "selection": "on device (sa_block_select)",
+                    "flops_basis": "selected blocks + selection scores"})
+        return cfg
+
+    def setup(self, nsets):
+        import torch
+        super().setup(nsets)
+        sc = self.sc
+        dev = torch.device("cuda")
+        T = sc.batch * sc.seq_len
+        self.qi, self.ki = _torch_bits(sc.index_q).to(dev), _torch_bits(sc.index_k).to(dev)
+        self.tabs = torch.empty((sc.num_index_heads, T, sc.topk), dtype=torch.int32,
+                                device=dev)
+
+    def launches_per_call(self):
+        return 2
+
+    def call(self, i, mode=None):
+        import attention_head_sinks_gb300 as sa
+        q, k, v, out, lse = self.sets[i % len(self.sets)]
+        c, sc = self.c, self.sc
+        sa.sa_block_select(self.qi, self.ki, sc.batch, sc.seq_len, sc.block_size, sc.topk,
+                           block_table=self.tabs)
+        sa.sa_block_sparse_fwd_index_heads(q, k, v, c.batch, c.seq_len, self.tabs,
+                                           c.block_size, self.cu, self.sinks,
+                                           self.mode if mode is None else mode, c.scale,
+                                           out=out, lse=lse)
+
+    def host_io(self):
+        import torch
+        c, sc = self.c, self.sc
+        host_in = [_torch_bits(x) for x in (c.q, c.k, c.v)] + \
+            [_torch_bits(sc.index_q), _torch_bits(sc.index_k), torch.from_numpy(c.cu_docs),
+             torch.from_numpy(c.sinks)]
+        out, lse = self.sets[0][3], self.sets[0][4]
+
+        def run(dev_in):
+            import attention_head_sinks_gb300 as sa
+            sa.sa_block_select(dev_in[3], dev_in[4], sc.batch, sc.seq_len, sc.block_size,
+                               sc.topk, block_table=self.tabs)
+            sa.sa_block_sparse_fwd_index_heads(dev_in[0], dev_in[1], dev_in[2], c.batch,
+                                               c.seq_len, self.tabs, c.block_size, dev_in[5],
+                                               dev_in[6], self.mode, c.scale, out=out,
+                                               lse=lse)
+        return host_in, [out, lse], run
+
+    def oracle(self, rows):
+        from oracle import sa_oracle
+        c, sc = self.c, self.sc
+        tabs, _ = sa_oracle.block_select(sc.index_q, sc.index_k, sc.batch, sc.seq_len,
+                                         sc.block_size, sc.topk, rows=rows)
+        sa_oracle.block_sparse_fwd_index_heads(c.q, c.k, c.v, c.batch, c.seq_len, tabs,
+                                               c.block_size, c.cu_docs, c.sinks, self.mode,
+                                               c.scale, rows=rows)
+
+
 RUNNERS = {
     "vision_window_16384tok": WindowRunner,
     "vision_window_4096tok": WindowRunner,
@@ -520,6 +684,8 @@ RUNNERS = {
     "mla_sparse_decode_fp8": IndexFp8Runner,
     "dsa_block_prefill": BlockRunner,
     "merge_window_16384tok": MergeRunner,
+    "dsa_block_select": SelectRunner,
+    "dsa_block_prefill_selected": SelectedBlockRunner,
 }
 
 
@@ -691,7 +857,7 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.steps is None:
-        args.steps = 500 if args.workload == "dsa_block_prefill" else 5000
+        args.steps = 500 if args.workload.startswith("dsa_block_prefill") else 5000
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -209,6 +209,51 @@ SA_API sa_status sa_block_sparse_fwd(const void* q, const void* k, const void* v
                                      void* stream);
 
 /*
+ * sa_block_sparse_fwd with one block selection per index head ([M3 CP
+ * sparse] _select_local_blocks: [batch, index_heads, sequence, key_blocks]).
+ * block_table is int32 [num_index_heads, batch * seq_len, topk_blocks] (the
+ * layout sa_block_select writes); query head h uses index head
+ * h / (num_q_heads / num_index_heads).  num_index_heads must divide
+ * num_kv_heads (the query heads of one KV head share one selection),
+ * otherwise SA_ERR_INVALID_ARG.  Everything else -- key sets, sink modes,
+ * layouts, supported sizes and errors -- as sa_block_sparse_fwd, which is
+ * this call with num_index_heads = 1.
+ */
+SA_API sa_status sa_block_sparse_fwd_index_heads(
+    const void* q, const void* k, const void* v, int32_t batch, int32_t seq_len,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    const int32_t* block_table, int32_t num_index_heads, int32_t topk_blocks,
+    int32_t block_size, const int32_t* cu_docs, int32_t num_docs, const float* sinks,
+    int32_t sink_mode, float softmax_scale, void* out, float* lse, void* stream);
+
+/*
+ * Top-k key-block selection from indexer scores, one selection per index
+ * head -- [M3 CP sparse] MiniMaxM3CPSparseAttention forward step 3 (top-k
+ * key blocks of each query from index q / k over the causal sequence of its
+ * batch row) and _select_local_blocks (one selection per index head;
+ * documents are not consulted -- their mask is applied in the attention).
+ * The page gives no score formula; this call takes: token score
+ * index_q[i, g] . index_k[j] (fp32 accumulation of the bf16 inputs); a
+ * block's score is the max over its keys; token i at row position p always
+ * selects its own block p / block_size, plus the topk_blocks - 1
+ * highest-scoring earlier blocks of its batch row (ties to the lower id); a
+ * token with at most topk_blocks causal blocks selects them all.  Scores
+ * that differ only in the last fp32 bits may rank either way.
+ *
+ *   index_q      bf16 [batch * seq_len, num_index_heads, index_dim]
+ *   index_k      bf16 [batch * seq_len, index_dim]  (one index key per token)
+ *   block_table  int32 [num_index_heads, batch * seq_len, topk_blocks]
+ *                (written: ascending block ids from the batch-row start,
+ *                -1 padded) -- the input of sa_block_sparse_fwd_index_heads
+ * Supported: index_dim = 128, block_size = 64, seq_len a multiple of 128,
+ * 1 <= topk_blocks <= 16, batch * seq_len < 2^31.  No workspace.
+ */
+SA_API sa_status sa_block_select(const void* index_q, const void* index_k, int32_t batch,
+                                 int32_t seq_len, int32_t num_index_heads,
+                                 int32_t index_dim, int32_t block_size,
+                                 int32_t topk_blocks, int32_t* block_table, void* stream);
+
+/*
  * Merge of two partial attention results over disjoint key sets of the same
  * queries (a cascade / split of one key set over calls) into the attention
  * over their union.  Each partial is the sink-free attention over its own

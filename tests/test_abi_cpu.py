@@ -222,3 +222,33 @@ def test_merge_rejects_bad_arguments(lib, kw, status, needle):
 
 def test_merge_empty_is_a_no_op(lib):
     assert _merge_call(lib, T=0) == 0
+
+
+def _select_call(lib, **kw):
+    a = dict(q=16, k=16, batch=2, S=8192, hi=4, di=128, bs=64, topk=16, tab=16)
+    a.update(kw)
+    return lib.sa_block_select(a["q"], a["k"], a["batch"], a["S"], a["hi"], a["di"], a["bs"],
+                               a["topk"], a["tab"], None)
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(q=None), 1, "NULL"),
+    (dict(tab=None), 1, "NULL"),
+    (dict(hi=0), 1, "bad sizes"),
+    (dict(topk=0), 1, "bad sizes"),
+    (dict(batch=1 << 20), 1, "2^31"),
+    (dict(k=24), 1, "misaligned"),
+])
+def test_block_select_rejects_bad_arguments(lib, kw, status, needle):
+    assert _select_call(lib, **kw) == status
+    assert needle in lib.sa_last_error().decode()
+
+
+def test_block_select_empty_is_a_no_op(lib):
+    assert _select_call(lib, batch=0) == 0
+
+
+def test_block_index_heads_must_divide_kv_heads(lib):
+    st = lib.sa_block_sparse_fwd_index_heads(16, 16, 16, 2, 8192, 32, 4, 128, 16, 3, 16, 64,
+                                             16, 6, 16, 2, 0.08, 16, 16, None)
+    assert st == 1 and "divide" in lib.sa_last_error().decode()
