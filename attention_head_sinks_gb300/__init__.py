@@ -38,10 +38,18 @@ def _dev_tensor(name, t, dtype, ndim=None):
     return t
 
 
-def _stream_handle(stream):
+def _stream_handle(stream, device=None):
+    """Raw cudaStream_t of ``stream`` (default: the current stream of
+    ``device``)."""
     torch = _torch()
-    s = torch.cuda.current_stream() if stream is None else stream
-    return s.cuda_stream
+    if stream is not None:
+        return stream.cuda_stream
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        idx = device.index if device is not None and device.index is not None \
+            else torch.cuda.current_device()
+        return raw(idx)
+    return torch.cuda.current_stream().cuda_stream
 
 
 def sa_varlen_window_fwd(q, k, v, cu_seqlens, window_left, window_right, sinks,
@@ -76,7 +84,7 @@ def sa_varlen_window_fwd(q, k, v, cu_seqlens, window_left, window_right, sinks,
         cu_seqlens.numel() - 1, T, hq, hkv, d, int(window_left),
         int(window_right), None if sinks is None else sinks.data_ptr(),
         int(sink_mode), float(softmax_scale), out.data_ptr(), lse.data_ptr(),
-        _stream_handle(stream)))
+        _stream_handle(stream, q.device)))
     return out, lse
 
 
@@ -128,7 +136,7 @@ def sa_sparse_index_fwd(q, kv_latent, indices, dv, sinks, sink_mode,
         indices.data_ptr(), topk, nq, hq,
         None if sinks is None else sinks.data_ptr(), int(sink_mode),
         float(softmax_scale), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes,
-        _stream_handle(stream)))
+        _stream_handle(stream, out.device)))
     return out, lse
 
 
@@ -175,7 +183,7 @@ def sa_sparse_index_fwd_fp8(q, kv_fp8, kv_scale, indices, dv, sinks, sink_mode,
         indices.data_ptr(), topk, nq, hq,
         None if sinks is None else sinks.data_ptr(), int(sink_mode),
         float(softmax_scale), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes,
-        _stream_handle(stream)))
+        _stream_handle(stream, out.device)))
     return out, lse
 
 
@@ -202,7 +210,8 @@ def sa_block_select(index_q, index_k, batch, seq_len, block_size, topk_blocks,
     from ._lib import check
     check(lib().sa_block_select(
         index_q.data_ptr(), index_k.data_ptr(), int(batch), int(seq_len), hi, di,
-        int(block_size), int(topk_blocks), block_table.data_ptr(), _stream_handle(stream)))
+        int(block_size), int(topk_blocks), block_table.data_ptr(),
+        _stream_handle(stream, block_table.device)))
     return block_table
 
 
@@ -239,7 +248,7 @@ def sa_block_sparse_fwd_index_heads(q, k, v, batch, seq_len, block_table, block_
         block_table.data_ptr(), block_table.shape[0], block_table.shape[2],
         int(block_size), cu_docs.data_ptr(), cu_docs.numel() - 1,
         None if sinks is None else sinks.data_ptr(), int(sink_mode),
-        float(softmax_scale), out.data_ptr(), lse.data_ptr(), _stream_handle(stream)))
+        float(softmax_scale), out.data_ptr(), lse.data_ptr(), _stream_handle(stream, out.device)))
     return out, lse
 
 
@@ -282,7 +291,7 @@ def sa_block_sparse_fwd(q, k, v, batch, seq_len, block_table, block_size,
         cu_docs.data_ptr(), cu_docs.numel() - 1,
         None if sinks is None else sinks.data_ptr(), int(sink_mode),
         float(softmax_scale), out.data_ptr(), lse.data_ptr(), None, 0,
-        _stream_handle(stream)))
+        _stream_handle(stream, out.device)))
     return out, lse
 
 
@@ -315,7 +324,7 @@ def sa_merge_attn_states(out_a, lse_a, out_b, lse_b, sinks, sink_mode, out=None,
     check(lib().sa_merge_attn_states(
         out_a.data_ptr(), lse_a.data_ptr(), out_b.data_ptr(), lse_b.data_ptr(), T, h, d,
         None if sinks is None else sinks.data_ptr(), int(sink_mode), out.data_ptr(),
-        lse.data_ptr(), _stream_handle(stream)))
+        lse.data_ptr(), _stream_handle(stream, out.device)))
     return out, lse
 
 

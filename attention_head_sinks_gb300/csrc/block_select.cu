@@ -316,9 +316,9 @@ sa_status launch_block_select(const SelectArgs& a) {
   p.err = device_error_word();
   const size_t smem = 1024 + (size_t)kHeadsPerCta * kSlabs * kQSlabBytes +
                       (size_t)kStages * kStageBytes;
-  cudaError_t e = cudaFuncSetAttribute(block_select_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  if (!set_dynamic_smem_once((const void*)block_select_kernel, (int)smem))
+    return fail(SA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(cudaGetLastError()));
+  cudaError_t e;
   const int64_t ctas = (int64_t)p.ntiles_q * a.batch * p.npairs;
   if (ctas >= ((int64_t)1 << 31))
     return fail(SA_ERR_UNSUPPORTED, "%s: %lld tiles", fn, (long long)ctas);

@@ -587,10 +587,9 @@ sa_status launch_typed(const BlockArgs& a) {
   const size_t smem = 1024 + 2 * kQSlab + (size_t)kStages * kStageBytes +
                       (size_t)kMaxUnion * 4 + (size_t)kMaxUnion * TW * 4;
   auto kern = block_sparse_fwd_kernel<G, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess)
-    return fail(SA_ERR_CUDA, "sa_block_sparse_fwd: %s", cudaGetErrorString(e));
+  if (!set_dynamic_smem_once((const void*)kern, (int)smem))
+    return fail(SA_ERR_CUDA, "sa_block_sparse_fwd: %s", cudaGetErrorString(cudaGetLastError()));
+  cudaError_t e;
   dim3 grid((unsigned)(T / TQ), (unsigned)a.num_kv_heads);
   kern<<<grid, kThreads, smem, a.stream>>>(tq, tk, tv, p);
   e = cudaGetLastError();

@@ -56,10 +56,55 @@ sa_status fail(sa_status st, const char* fmt, ...) {
   return st;
 }
 
+namespace {
+// Encoded maps of recent calls, per host thread.  An encoding is a pure
+// function of its arguments (no device state), so a call with the same
+// arguments -- the same buffers, shapes and boxes, as in a serving or
+// training loop -- reuses it instead of encoding again.
+struct MapKey {
+  const void* base;
+  uint64_t dims[5], strides[4];
+  uint32_t box[5];
+  int32_t dtype, rank, swizzle, promotion;
+  bool operator==(const MapKey& o) const { return memcmp(this, &o, sizeof *this) == 0; }
+};
+struct MapEntry {
+  bool used;
+  MapKey key;
+  CUtensorMap map;
+};
+constexpr int kMapCacheSlots = 64;
+thread_local MapEntry t_map_cache[kMapCacheSlots];
+
+uint32_t map_slot(const MapKey& k) {
+  const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+  uint32_t h = 2166136261u;  // FNV-1a
+  for (size_t i = 0; i < sizeof k; ++i) h = (h ^ b[i]) * 16777619u;
+  return h % kMapCacheSlots;
+}
+}  // namespace
+
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank,
                   const void* base, const uint64_t* dims,
                   const uint64_t* strides_bytes, const uint32_t* box,
                   CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promotion) {
+  MapKey key;
+  memset(&key, 0, sizeof key);  // padding bytes take part in the comparison
+  key.base = base;
+  for (int i = 0; i < rank && i < 5; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+    if (i + 1 < rank) key.strides[i] = strides_bytes[i];
+  }
+  key.dtype = (int32_t)dtype;
+  key.rank = rank;
+  key.swizzle = (int32_t)swizzle;
+  key.promotion = (int32_t)promotion;
+  MapEntry& slot = t_map_cache[map_slot(key)];
+  if (slot.used && slot.key == key) {
+    *map = slot.map;
+    return true;
+  }
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable (no CUDA driver?)");
@@ -76,6 +121,36 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank,
     fail(SA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return false;
   }
+  slot.used = true;
+  slot.key = key;
+  slot.map = *map;
+  return true;
+}
+
+bool set_dynamic_smem_once(const void* func, int bytes) {
+  // (kernel, device) pairs whose attribute is already at least `bytes`
+  struct Done {
+    const void* func;
+    int dev;
+    int bytes;
+  };
+  static std::mutex mu;
+  static Done done[256];
+  static int ndone = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < ndone; ++i)
+    if (done[i].func == func && done[i].dev == dev && done[i].bytes >= bytes) return true;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  for (int i = 0; i < ndone; ++i)
+    if (done[i].func == func && done[i].dev == dev) {
+      done[i].bytes = bytes;
+      return true;
+    }
+  if (ndone < 256) done[ndone++] = Done{func, dev, bytes};
   return true;
 }
 

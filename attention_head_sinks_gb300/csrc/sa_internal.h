@@ -24,6 +24,11 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank,
                   CUtensorMapSwizzle swizzle,
                   CUtensorMapL2promotion promotion = CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 
+// Raise a kernel's dynamic shared memory limit to `bytes` on the current
+// device, calling the runtime only the first time per (kernel, device, size).
+// False (with the runtime's error pending) when the runtime refuses.
+bool set_dynamic_smem_once(const void* func, int bytes);
+
 // Address of this device's error word (a __device__ variable).
 uint32_t* device_error_word();
 

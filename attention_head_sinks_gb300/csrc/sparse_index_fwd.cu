@@ -1002,7 +1002,7 @@ struct CombineSmem {
 };
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 sparse_index_combine_kernel(const IndexParams p) {
   __shared__ __align__(16) CombineSmem sm;
   griddep_wait();  // the attend kernel's partials are complete
@@ -1196,8 +1196,8 @@ sa_status launch_typed(const IndexArgs& a) {
 
   const size_t smem = 1024 + (size_t)kNumSlots * kSlotBytes + 2 * (size_t)kSlabBytesQ;
   auto kern = sparse_index_fwd_kernel<MODE, FP8>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  if (!set_dynamic_smem_once((const void*)kern, (int)smem))
+    return fail(SA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(cudaGetLastError()));
   // at most one item per (query, 256 index slots)
   const unsigned items = (unsigned)((int64_t)a.num_queries * nslices * p.nhb);
   e = launch_dependent(kern, dim3(items), dim3(kThreads), smem, a.stream, tq, a.kv, p);
@@ -1230,8 +1230,8 @@ sa_status launch_typed(const IndexArgs& a) {
     const unsigned g1 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(max_units, num_sms()));
     const size_t smem_c = 128 + kFcStages * sizeof(FcStage);
     auto kc = sparse_index_combine_tma_kernel<MODE>;
-    e = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_c);
-    if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    if (!set_dynamic_smem_once((const void*)kc, (int)smem_c))
+      return fail(SA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(cudaGetLastError()));
     e = launch_dependent(kc, dim3(g1), dim3(kThreads), smem_c, a.stream, tp, tp1, tml, p);
     if (e != cudaSuccess)
       return fail(SA_ERR_CUDA, "%s combine launch: %s", fn, cudaGetErrorString(e));
@@ -1242,7 +1242,7 @@ sa_status launch_typed(const IndexArgs& a) {
                              (p.head_stride / 32);
       const int64_t per_cta = kThreads / 32;
       const unsigned g2 = (unsigned)std::max<int64_t>(
-          1, std::min<int64_t>((wunits + per_cta - 1) / per_cta, 2 * num_sms()));
+          1, std::min<int64_t>((wunits + per_cta - 1) / per_cta, num_sms()));
       e = launch_dependent(sparse_index_combine_kernel<MODE>, dim3(g2), dim3(kThreads), 0,
                            a.stream, p);
       if (e != cudaSuccess)

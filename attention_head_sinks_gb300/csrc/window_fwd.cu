@@ -224,10 +224,9 @@ sa_status launch_typed(const WindowArgs& a, int nk) {
   size_t smem = 1024 + (size_t)(128 + 2 * nk) * D * 2;
   if (smem < 80 * 1024) smem = 80 * 1024;
   auto kern = window_fwd_kernel<D, G, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(
-      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess)
-    return fail(SA_ERR_CUDA, "sa_varlen_window_fwd: %s", cudaGetErrorString(e));
+  if (!set_dynamic_smem_once((const void*)kern, (int)smem))
+    return fail(SA_ERR_CUDA, "sa_varlen_window_fwd: %s", cudaGetErrorString(cudaGetLastError()));
+  cudaError_t e;
   dim3 grid((unsigned)((a.total_tokens + TQ - 1) / TQ), (unsigned)a.num_kv_heads);
   kern<<<grid, 128, smem, a.stream>>>(tq, tk, tv, p);
   e = cudaGetLastError();

@@ -402,10 +402,9 @@ sa_status launch_ring_typed(const WindowArgs& a, int nbt, int bf_off) {
   p.lse = a.lse;
   p.err = device_error_word();
   auto kern = window_ring_kernel<D, G, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)S::SMEM);
-  if (e != cudaSuccess)
-    return fail(SA_ERR_CUDA, "sa_varlen_window_fwd: %s", cudaGetErrorString(e));
+  if (!set_dynamic_smem_once((const void*)kern, (int)S::SMEM))
+    return fail(SA_ERR_CUDA, "sa_varlen_window_fwd: %s", cudaGetErrorString(cudaGetLastError()));
+  cudaError_t e;
   p.num_kv_heads = a.num_kv_heads;
   p.chunks = num_sms() / a.num_kv_heads;
   if (p.chunks < 1) p.chunks = 1;

@@ -888,24 +888,41 @@ def main():
     barrier()
 
     def timed(mode, steps):
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        """The contract's timed region: K calls through the public API,
+        bracketed by barrier + synchronize, CUDA events on the launching
+        stream at both ends.  Nothing else is enqueued in between."""
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         e0.record()
         for i in range(steps):
+            runner.call(i, mode)
+        e1.record()
+        barrier()
+        return e0.elapsed_time(e1)
+
+    def device_times(mode, steps):
+        """Device time of each call (CUDA events around it on the launching
+        stream), with the calls queued behind a device-side sleep so that the
+        host's enqueue time never appears as idle time between the events."""
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        barrier()
+        sleep = getattr(torch.cuda, "_sleep", None)
+        if sleep is not None:  # about 60 us of host time per queued call
+            sleep(int(2.0e9 * (0.005 + steps * 60e-6)))
+        for i in range(steps):
             starts[i].record()
             runner.call(i, mode)
             ends[i].record()
-        e1.record()
         barrier()
-        per = [s.elapsed_time(e) * 1000.0 for s, e in zip(starts, ends)]
-        return e0.elapsed_time(e1), per
+        return [s_.elapsed_time(e_) * 1000.0 for s_, e_ in zip(starts, ends)]
 
     sampler = ClockSampler(gpu_uuid())
-    total_ms, per = timed(runner.mode, args.steps)
+    total_ms = timed(runner.mode, args.steps)
     clocks = sampler.stop()
-    _, per_none = timed(W.SINK_NONE, max(args.steps // 4, 10))
+    ndev = min(args.steps, 500)
+    per = device_times(runner.mode, ndev)
+    per_none = device_times(W.SINK_NONE, max(ndev // 2, 10))
 
     step_ms = total_ms / args.steps
     if dist is not None:

@@ -76,6 +76,15 @@ def test_small_selection(hi, topk):
     assert mism <= 0.01 * hi * 768, mism
 
 
+@pytest.mark.parametrize("batch,seq_len", [(1, 128), (3, 128), (1, 640)])
+def test_short_rows_and_batches(batch, seq_len):
+    # fewer tokens than one 256-key tile (the key box runs past the tensor),
+    # rows that end inside a key tile, and a batch of one-tile rows
+    c = W.select_case(batch, seq_len, 2, 128, 64, 3, seed=80 + batch + seq_len)
+    got = gpu_select(c)
+    assert check_selection(c, got) <= 0.01 * 2 * batch * seq_len
+
+
 def test_dsa_block_select_sampled_rows():
     c = W.dsa_block_select()
     got = gpu_select(c)
