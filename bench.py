@@ -776,6 +776,23 @@ def recorded_traffic(workload, src_hash):
     return None
 
 
+def max_over_ranks(value, dist, device):
+    """The slowest rank's value (the whole job's step time); ``value`` itself
+    without a process group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value_us(step_ms, world):
+    """us per call over the whole job: every rank runs one call per step, so
+    the job completes ``world`` calls per slowest-rank step."""
+    return step_ms * 1000.0 / world
+
+
 # ----------------------------------------------------------------------------
 # CPU oracle (baseline and reference arm)
 # ----------------------------------------------------------------------------
@@ -924,11 +941,7 @@ def main():
     per = device_times(runner.mode, ndev)
     per_none = device_times(W.SINK_NONE, max(ndev // 2, 10))
 
-    step_ms = total_ms / args.steps
-    if dist is not None:
-        t = torch.tensor([step_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(total_ms / args.steps, dist, "cuda")
     kern_us = statistics.mean(per)
     kern_us_none = statistics.mean(per_none)
 
@@ -981,7 +994,7 @@ def main():
         other = {"alg_gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm_peak, 4)}
     roof.update({"peak_source": peak_src, "alg_bytes": nbytes, "alg_flops": flops,
                  "kernel_us": round(kern_us, 3), "source_hash": src_hash})
-    value_us = step_ms * 1000.0 / world
+    value_us = job_value_us(step_ms, world)
     cfg = runner.config()
     cfg.update({"global_batch": world, "parallelism": "replicas x%d" % world,
                 "l2": "%d rotating input sets (%.0f MB touched) > 129 MB L2" %
