@@ -14,7 +14,8 @@ from .workloads import SINK_KEY0_BIAS, SINK_NONE, SINK_NULL_LOGIT  # noqa: F401
 __all__ = ["sa_varlen_window_fwd", "sa_sparse_index_fwd", "sa_sparse_index_fwd_fp8",
            "sa_block_sparse_fwd", "sa_block_sparse_fwd_index_heads", "sa_block_select",
            "sa_merge_attn_states",
-           "sa_sparse_index_workspace_size", "sa_device_error", "sa_version", "SAError",
+           "sa_sparse_index_workspace_size", "sa_device_error", "sa_check_wait_expiry",
+           "sa_version", "SAError",
            "SINK_NONE", "SINK_KEY0_BIAS", "SINK_NULL_LOGIT"]
 
 
@@ -335,6 +336,13 @@ def sa_device_error() -> int:
     code = ctypes.c_uint32(0)
     check(lib().sa_device_error(ctypes.byref(code)))
     return int(code.value)
+
+
+def sa_check_wait_expiry(stream=None) -> None:
+    """Enqueue one kernel whose bounded wait runs out (C:
+    ``sa_check_wait_expiry``); ``sa_device_error()`` then returns 32."""
+    from ._lib import check
+    check(lib().sa_check_wait_expiry(_stream_handle(stream)))
 
 
 def sa_version() -> int:

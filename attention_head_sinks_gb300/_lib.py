@@ -49,6 +49,7 @@ SIGNATURES = {
         _P, _P, _P, _P, _I64, _I32, _I32, _P, _I32, _P, _P, _P]),
     "sa_last_error": (ctypes.c_char_p, []),
     "sa_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "sa_check_wait_expiry": (ctypes.c_int, [_P]),
     "sa_version": (ctypes.c_uint32, []),
 }
 

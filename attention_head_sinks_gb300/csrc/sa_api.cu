@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "sa_internal.h"
+#include "sa_ptx.cuh"
 
 namespace sa {
 
@@ -188,6 +189,31 @@ extern "C" {
 const char* sa_last_error(void) { return sa::t_last_error; }
 
 uint32_t sa_version(void) { return (0u << 16) | 1u; }
+
+namespace sa {
+namespace {
+// One bounded wait on an mbarrier that nothing ever arrives on: it runs out
+// after kWaitLimitNs, records kErrWaitCheck and the kernel returns normally.
+__global__ void wait_expiry_kernel(uint32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_wait(&bar, 0, err, kErrWaitCheck);
+  }
+}
+}  // namespace
+}  // namespace sa
+
+sa_status sa_check_wait_expiry(void* stream) {
+  uint32_t* err = sa::device_error_word();
+  if (!err) return fail(SA_ERR_CUDA, "sa_check_wait_expiry: no usable CUDA device");
+  sa::wait_expiry_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return fail(SA_ERR_CUDA, "sa_check_wait_expiry launch: %s", cudaGetErrorString(e));
+  return SA_OK;
+}
 
 sa_status sa_device_error(uint32_t* code) {
   if (!code) return fail(SA_ERR_INVALID_ARG, "sa_device_error: code is NULL");

@@ -19,6 +19,7 @@ enum : uint32_t {
   kErrWaitFree = 1u << 2,   // a buffer was never released
   kErrWaitDrain = 1u << 3,  // in-flight copies did not drain before exit
   kErrConfig = 1u << 4,     // a launch-time invariant did not hold
+  kErrWaitCheck = 1u << 5,  // sa_check_wait_expiry's wait (expected to run out)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -313,10 +313,21 @@ SA_API const char* sa_last_error(void);
 
 /*
  * Device error word of the current device: bits set by kernels whose bounded
- * waits ran out (1 load, 2 MMA, 4 buffer release, 8 drain, 16 config).
- * Synchronises the device, reads the word into *code and clears it.
+ * waits ran out (1 load, 2 MMA, 4 buffer release, 8 drain, 16 config,
+ * 32 the wait of sa_check_wait_expiry).  Synchronises the device, reads the
+ * word into *code and clears it.
  */
 SA_API sa_status sa_device_error(uint32_t* code);
+
+/*
+ * Exercises the failure path of the bounded waits without faulting anything:
+ * enqueues one kernel whose thread waits on an mbarrier that nothing ever
+ * arrives on.  The wait runs out after about one second, the kernel sets
+ * bit 32 of the device error word and returns normally; the context stays
+ * usable.  A caller checks the mechanism with this call followed by
+ * sa_device_error (expect 32).
+ */
+SA_API sa_status sa_check_wait_expiry(void* stream);
 
 /* Library version as (major << 16) | minor. */
 SA_API uint32_t sa_version(void);
