@@ -44,10 +44,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kD = 128;
 constexpr int kBlk = 64;
 constexpr int kStepKeys = 128;                 // two blocks per step
-constexpr int kStages = 2;
+constexpr int kMaxKStages = 3;                 // K ring (fewer where shared memory is short)
+constexpr int kVStages = 2;                    // V ring
 constexpr int kQSlab = 128 * 128;              // 128 rows x 64 dims, 16 KB
 constexpr int kKVSlab = kStepKeys * 128;       // 128 keys x 64 dims, 16 KB
-constexpr int kStageBytes = 4 * kKVSlab;       // K: 2 slabs, V: 2 slabs
+constexpr int kStepBytes = 2 * kKVSlab;        // K (or V) of one step: 2 slabs
 constexpr int kMaxUnion = 2048;
 constexpr int kMaxBitmapWords = 512;           // 16384 blocks per batch row
 constexpr int kTmemCols = 512;
@@ -75,8 +76,10 @@ struct BlockParams {
 
 struct __align__(8) BlockSmemCtl {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t k_full[kMaxKStages];
+  uint64_t k_empty[kMaxKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done;
@@ -126,6 +129,16 @@ __device__ __forceinline__ int upper_doc(const int32_t* cu, int n, int t) {
   return __ldg(cu + lo);
 }
 
+// Dynamic shared memory of a tile with KST K stages: Q, the K and V rings,
+// the union list and its token masks.
+__host__ __device__ constexpr size_t block_smem_bytes(int G, int KST) {
+  return 1024 + 2 * (size_t)kQSlab + (size_t)KST * kStepBytes + (size_t)kVStages * kStepBytes +
+         (size_t)kMaxUnion * 4 + (size_t)kMaxUnion * ((128 / G) > 32 ? (128 / G) / 32 : 1) * 4;
+}
+__host__ __device__ constexpr int block_k_stages(int G) {
+  return block_smem_bytes(G, 3) + sizeof(BlockSmemCtl) <= 227 * 1024 ? 3 : 2;
+}
+
 template <int G, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -139,8 +152,10 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                                  // 2 x 16 KB
-  uint8_t* sKV = sQ + 2 * kQSlab;                      // stages x 64 KB
-  int32_t* ulist = reinterpret_cast<int32_t*>(sKV + kStages * kStageBytes);
+  constexpr int KST = block_k_stages(G);
+  uint8_t* sK = sQ + 2 * kQSlab;                       // KST x 32 KB
+  uint8_t* sV = sK + KST * kStepBytes;                 // 2 x 32 KB
+  int32_t* ulist = reinterpret_cast<int32_t*>(sV + kVStages * kStepBytes);
   uint32_t* tokmask = reinterpret_cast<uint32_t*>(ulist + kMaxUnion);
 
   const int tid = threadIdx.x;
@@ -186,9 +201,13 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   for (int w = tid; w < nwords; w += kThreads) ctl.bitmap[w] = 0u;
   if (tid == 0) {
     mbar_init(&ctl.q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ctl.kv_full[s], 1);
-      mbar_init(&ctl.kv_empty[s], 1);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(&ctl.k_full[s], 1);
+      mbar_init(&ctl.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&ctl.v_full[s], 1);
+      mbar_init(&ctl.v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl.s_full[b], 1);
@@ -278,44 +297,52 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int nsteps = (U + 1) >> 1;
   bool ok = true;
 
-  if (tid == 0 && nsteps > 0) {
-    // ---- producer (Q was loaded during the set-up) ----------------------------
+  // K and V of step j stream through separate rings with their own producer
+  // threads: K (needed first, by S) runs KST steps ahead of the MMAs, V (needed
+  // after the softmax) two.
+  auto produce = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* empty,
+                     int nst) {
     int issued = 0;
+    bool pok = true;
     for (int j = 0; j < nsteps; ++j) {
-      const int st = j & 1;
-      if (j >= kStages) {
-        ok = mbar_wait(&ctl.kv_empty[st], ((j >> 1) - 1) & 1, p.err, kErrWaitFree);
-        if (!ok) break;
+      const int st = j % nst;
+      if (j >= nst) {
+        pok = mbar_wait(&empty[st], ((j / nst) - 1) & 1, p.err, kErrWaitFree);
+        if (!pok) break;
       }
       const int nb = min(2, U - 2 * j);
-      uint8_t* stage = sKV + st * kStageBytes;
-      mbar_arrive_expect_tx(&ctl.kv_full[st], (uint32_t)nb * 4u * (kBlk * 128));
+      uint8_t* stage = ring + st * kStepBytes;
+      mbar_arrive_expect_tx(&full[st], (uint32_t)nb * 2u * (kBlk * 128));
       for (int bi = 0; bi < nb; ++bi) {
         const int kpos = row_start + ulist[2 * j + bi] * kBlk;
-        for (int s = 0; s < 2; ++s) {
-          tma_load_3d(stage + s * kKVSlab + bi * (kBlk * 128), &tm_k, &ctl.kv_full[st],
-                      64 * s, g, kpos);
-          tma_load_3d(stage + (2 + s) * kKVSlab + bi * (kBlk * 128), &tm_v, &ctl.kv_full[st],
-                      64 * s, g, kpos);
-        }
+        for (int s = 0; s < 2; ++s)
+          tma_load_3d(stage + s * kKVSlab + bi * (kBlk * 128), map, &full[st], 64 * s, g, kpos);
       }
       issued = j + 1;
     }
-    if (!ok) {
+    if (!pok) {
       // bounded drain of the copies still in flight
-      for (int j = max(0, issued - kStages); j < issued; ++j)
-        mbar_wait(&ctl.kv_full[j & 1], (j >> 1) & 1, p.err, kErrWaitDrain);
+      for (int j = max(0, issued - nst); j < issued; ++j)
+        mbar_wait(&full[j % nst], (j / nst) & 1, p.err, kErrWaitDrain);
     }
+  };
+  if (tid == 0 && nsteps > 0) {
+    // ---- K producer (Q was loaded during the set-up) --------------------------
+    produce(&tm_k, sK, ctl.k_full, ctl.k_empty, KST);
+  } else if (tid == 96 && nsteps > 0) {
+    // ---- V producer ------------------------------------------------------------
+    produce(&tm_v, sV, ctl.v_full, ctl.v_empty, kVStages);
   } else if (tid == 32 && nsteps > 0) {
     // ---- MMA issuer ----------------------------------------------------------
     ok = mbar_wait(&ctl.q_full, 0, p.err, kErrWaitLoad);
     auto issue_s = [&](int j) -> bool {
-      const int st = j & 1;
-      if (!mbar_wait(&ctl.kv_full[st], (j >> 1) & 1, p.err, kErrWaitLoad)) return false;
+      const int st = j & 1;  // S buffer
+      const int ks = j % KST;
+      if (!mbar_wait(&ctl.k_full[ks], (j / KST) & 1, p.err, kErrWaitLoad)) return false;
       tc_fence_after();
       const int nb = min(2, U - 2 * j);
       const uint32_t idesc = idesc_bf16(128, nb * kBlk, false);
-      const uint8_t* kst = sKV + st * kStageBytes;
+      const uint8_t* kst = sK + ks * kStepBytes;
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
 #pragma unroll
@@ -325,6 +352,7 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
           mma_ss(tmem + (uint32_t)(st * 128), a, b, idesc, (s | kk) ? 1u : 0u);
         }
       }
+      mma_commit(&ctl.k_empty[ks]);
       mma_commit(&ctl.s_full[st]);
       return true;
     };
@@ -338,16 +366,19 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       ok = mbar_wait(&ctl.p_full[st], (j >> 1) & 1, p.err, kErrWaitMma);
       if (!ok) break;
       tc_fence_after();
+      ok = mbar_wait(&ctl.v_full[st], (j >> 1) & 1, p.err, kErrWaitLoad);
+      if (!ok) break;
+      tc_fence_after();
       const int nb = min(2, U - 2 * j);
       const uint32_t idesc = idesc_bf16(128, kD, true);
-      const uint8_t* vst = sKV + st * kStageBytes + 2 * kKVSlab;
+      const uint8_t* vst = sV + st * kStepBytes;
       for (int kk = 0; kk < nb * kBlk / 16; ++kk) {
         const uint64_t b = smem_desc(smem_u32(vst) + kk * 16 * 128, kKVSlab, 1024, kLayoutSw128);
         // P of block kk / 4 sits in the first half of that block's S columns
         mma_ts(tmem + kColO, tmem + (uint32_t)(st * 128 + 64 * (kk >> 2) + 8 * (kk & 3)), b, idesc,
                (j > 0 || kk > 0) ? 1u : 0u);
       }
-      mma_commit(&ctl.kv_empty[st]);
+      mma_commit(&ctl.v_empty[st]);
       mma_commit(&ctl.o_done);
     }
   } else if (warp >= 4) {
@@ -552,7 +583,8 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 template <int G, int MODE>
 sa_status launch_typed(const BlockArgs& a) {
   constexpr int TQ = 128 / G;
-  constexpr int TW = TQ > 32 ? TQ / 32 : 1;
+  static_assert(block_smem_bytes(G, block_k_stages(G)) + sizeof(BlockSmemCtl) <= 227 * 1024,
+                "shared memory");
   const int64_t T = (int64_t)a.batch * a.seq_len;
   CUtensorMap tq, tk, tv;
   const uint64_t dq[3] = {(uint64_t)kD, (uint64_t)a.num_q_heads, (uint64_t)T};
@@ -584,8 +616,7 @@ sa_status launch_typed(const BlockArgs& a) {
   p.out = reinterpret_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.err = device_error_word();
-  const size_t smem = 1024 + 2 * kQSlab + (size_t)kStages * kStageBytes +
-                      (size_t)kMaxUnion * 4 + (size_t)kMaxUnion * TW * 4;
+  const size_t smem = block_smem_bytes(G, block_k_stages(G));
   auto kern = block_sparse_fwd_kernel<G, MODE>;
   if (!set_dynamic_smem_once((const void*)kern, (int)smem))
     return fail(SA_ERR_CUDA, "sa_block_sparse_fwd: %s", cudaGetErrorString(cudaGetLastError()));
