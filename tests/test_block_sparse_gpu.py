@@ -155,3 +155,16 @@ def test_zero_key0_sink_is_bitwise_no_sink():
     o1, l1 = gpu_run(c, KEY0, sinks=np.zeros_like(c.sinks))
     assert torch.equal(o0.view(torch.int16), o1.view(torch.int16))
     assert torch.equal(l0, l1)
+
+
+@pytest.mark.parametrize("docs_per_row", [200, 300])
+@pytest.mark.parametrize("mode", [NULL, KEY0])
+def test_many_documents(docs_per_row, mode):
+    # hundreds of short documents: most key blocks are cut by a document
+    # start, most tokens see only part of their selected blocks
+    c = W.block_case(1, 4096, 16, 4, 128, 64, 8, docs_per_row, (-2.2, 2.49), mode,
+                     seed=4000 + docs_per_row)
+    out, lse = gpu_run(c, mode)
+    ro, rl = oracle_run(c, mode)
+    rel, dl = compare(out, lse, ro, rl)
+    assert rel <= REL_L2_TOL and dl <= LSE_TOL, (docs_per_row, mode, rel, dl)
