@@ -31,6 +31,8 @@
 // The running max is rescaled lazily: O and l are rescaled only when a row's
 // max grows by more than 2^8, so P stays below 256.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 #include <math.h>
 
 #include "sa_internal.h"
@@ -49,7 +51,7 @@ constexpr int kVStages = 2;                    // V ring
 constexpr int kQSlab = 128 * 128;              // 128 rows x 64 dims, 16 KB
 constexpr int kKVSlab = kStepKeys * 128;       // 128 keys x 64 dims, 16 KB
 constexpr int kStepBytes = 2 * kKVSlab;        // K (or V) of one step: 2 slabs
-constexpr int kMaxUnion = 2048;
+constexpr int kMaxUnion = 1024;                // union blocks per tile (per metadata buffer)
 constexpr int kMaxBitmapWords = 512;           // 16384 blocks per batch row
 constexpr int kTmemCols = 512;
 constexpr int kColO = 256;
@@ -67,6 +69,7 @@ struct BlockParams {
   const int32_t* cu_docs;
   int32_t num_docs;
   int32_t num_q_heads;
+  int32_t num_kv_heads;
   const float* sinks;
   float scale_log2;
   __nv_bfloat16* out;  // [T, Hq, 128]
@@ -75,22 +78,29 @@ struct BlockParams {
 };
 
 struct __align__(8) BlockSmemCtl {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t k_full[kMaxKStages];
   uint64_t k_empty[kMaxKStages];
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t o_done;
+  uint64_t o_done;          // one phase per step: O += P V of that step complete
+  uint64_t o_free;          // one phase per tile: its epilogue has read O
+  uint64_t meta_full[2];    // tile metadata buffer [tile parity] written
+  uint64_t meta_empty[2];   // ... and read by every role
   uint32_t tmem_base;
-  int32_t nunion;
-  float red_m[2][2][128];  // [step parity][part][row]: row max exchange
-  float red_l[2][128];     // [part][row]: row sums at the end
-  int32_t tok_pos[128];  // row-local position (-1 past the last token)
-  int32_t tok_lo[128];   // row-local start of the token's document
-  int32_t tok_k0[128];   // KEY0_BIAS key: row-local document start, -1 if before the row
-  uint32_t bitmap[kMaxBitmapWords];
+  int32_t abort_flag;       // a role's bounded wait ran out: every role stops
+  int32_t sm_stop[2];       // the softmax warps' stop decision, by checkpoint parity
+  int32_t nunion[2];
+  float red_m[2][2][128];   // [step parity][part][row]: row max exchange
+  float red_l[2][2][128];   // [tile parity][part][row]: row sums at the end
+  // per tile parity: row-local position (-1 past the last token), row-local
+  // start of the token's document, KEY0_BIAS key (-1 if before the row)
+  int32_t tok_pos[2][128];
+  int32_t tok_lo[2][128];
+  int32_t tok_k0[2][128];
+  uint32_t bitmap[kMaxBitmapWords];  // scratch of the metadata warp
   int32_t prefix[kMaxBitmapWords];
 };
 
@@ -129,11 +139,12 @@ __device__ __forceinline__ int upper_doc(const int32_t* cu, int n, int t) {
   return __ldg(cu + lo);
 }
 
-// Dynamic shared memory of a tile with KST K stages: Q, the K and V rings,
-// the union list and its token masks.
+// Dynamic shared memory with KST K stages: Q, the K and V rings, and two
+// metadata buffers (union list and its token masks).
 __host__ __device__ constexpr size_t block_smem_bytes(int G, int KST) {
   return 1024 + 2 * (size_t)kQSlab + (size_t)KST * kStepBytes + (size_t)kVStages * kStepBytes +
-         (size_t)kMaxUnion * 4 + (size_t)kMaxUnion * ((128 / G) > 32 ? (128 / G) / 32 : 1) * 4;
+         2 * ((size_t)kMaxUnion * 4 +
+              (size_t)kMaxUnion * ((128 / G) > 32 ? (128 / G) / 32 : 1) * 4);
 }
 __host__ __device__ constexpr int block_k_stages(int G) {
   return block_smem_bytes(G, 3) + sizeof(BlockSmemCtl) <= 227 * 1024 ? 3 : 2;
@@ -147,60 +158,33 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const BlockParams p) {
   constexpr int TQ = 128 / G;
   constexpr int TW = TQ > 32 ? TQ / 32 : 1;  // token-mask words per block
+  constexpr int KST = block_k_stages(G);
   extern __shared__ uint8_t smem_raw[];
   __shared__ BlockSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                                  // 2 x 16 KB
-  constexpr int KST = block_k_stages(G);
   uint8_t* sK = sQ + 2 * kQSlab;                       // KST x 32 KB
   uint8_t* sV = sK + KST * kStepBytes;                 // 2 x 32 KB
-  int32_t* ulist = reinterpret_cast<int32_t*>(sV + kVStages * kStepBytes);
-  uint32_t* tokmask = reinterpret_cast<uint32_t*>(ulist + kMaxUnion);
+  int32_t* ulist2 = reinterpret_cast<int32_t*>(sV + kVStages * kStepBytes);   // [2][kMaxUnion]
+  uint32_t* tokmask2 = reinterpret_cast<uint32_t*>(ulist2 + 2 * kMaxUnion);  // [2][kMaxUnion*TW]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int g = blockIdx.y;
-  const int tok0 = blockIdx.x * TQ;
-  const int row_start = (tok0 / p.seq_len) * p.seq_len;
+  // tiles of this CTA: blockIdx.x + n * gridDim.x over (KV head, token tile)
+  const int ntx = p.total_tokens / TQ;
+  const int ntiles = ntx * p.num_kv_heads;
+  const int nmine = (ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  auto tile_of = [&](int n, int& g, int& tok0) {
+    const int tt = (int)blockIdx.x + n * (int)gridDim.x;
+    g = tt / ntx;
+    tok0 = (tt - g * ntx) * TQ;
+  };
   const int nwords = (p.nblocks + 31) >> 5;
 
-  // ---- tile metadata: token positions, union of live blocks ---------------
-  // Every global read of the set-up is issued first (this thread's block-table
-  // entries, kept in registers for both passes below, and the document start
-  // of the tile's tokens); barrier set-up, the TMEM allocation and the Q load
-  // overlap them.
-  constexpr int kPairsPerThread = (kMaxUnion + kThreads - 1) / kThreads;
-  const int npairs = TQ * p.topk;  // <= kMaxUnion (checked on the host)
-  // the selection of this KV head's index head
-  const int32_t* table = p.table + (int64_t)(g / p.kv_per_index_head) * p.table_head_stride;
-  int32_t sel[kPairsPerThread];
-#pragma unroll
-  for (int k = 0; k < kPairsPerThread; ++k) {
-    const int w = tid + k * kThreads;
-    sel[k] = -1;
-    if (w < npairs) {
-      const int i = w / p.topk;
-      if (tok0 + i < p.total_tokens)
-        sel[k] = __ldg(table + (int64_t)(tok0 + i) * p.topk + (w - i * p.topk));
-    }
-  }
-  if (tid < TQ) {
-    const int t = tok0 + tid;
-    if (t < p.total_tokens) {
-      const int doc = upper_doc(p.cu_docs, p.num_docs, t);
-      ctl.tok_pos[tid] = t - row_start;
-      ctl.tok_lo[tid] = max(doc - row_start, 0);
-      ctl.tok_k0[tid] = doc >= row_start ? doc - row_start : -1;
-    } else {
-      ctl.tok_pos[tid] = -1;
-      ctl.tok_lo[tid] = 0;
-      ctl.tok_k0[tid] = -1;
-    }
-  }
-  for (int w = tid; w < nwords; w += kThreads) ctl.bitmap[w] = 0u;
   if (tid == 0) {
     mbar_init(&ctl.q_full, 1);
+    mbar_init(&ctl.q_empty, 1);
     for (int s = 0; s < KST; ++s) {
       mbar_init(&ctl.k_full[s], 1);
       mbar_init(&ctl.k_empty[s], 1);
@@ -212,174 +196,277 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl.s_full[b], 1);
       mbar_init(&ctl.p_full[b], 8);
+      mbar_init(&ctl.meta_full[b], 1);
+      mbar_init(&ctl.meta_empty[b], 11);  // 8 softmax warps, K, V, MMA
     }
     mbar_init(&ctl.o_done, 1);
+    mbar_init(&ctl.o_free, 8);
+    ctl.abort_flag = 0;
+    ctl.sm_stop[0] = ctl.sm_stop[1] = 0;
     fence_mbar_init();
-    // Q of the tile does not depend on the key set: load it now
     tma_prefetch_map(&tm_q);
     tma_prefetch_map(&tm_k);
     tma_prefetch_map(&tm_v);
-    mbar_arrive_expect_tx(&ctl.q_full, 2 * kQSlab);
-    for (int s2 = 0; s2 < 2; ++s2)
-      tma_load_3d(sQ + s2 * kQSlab, &tm_q, &ctl.q_full, 64 * s2, g * G, tok0);
   }
   if (warp == 2) {
     tmem_alloc(&ctl.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  __syncthreads();
-  // live selection of pair w = (token i, entry): block b intersects [doc start, pos]
-  auto live_block = [&](int k, int& i, int& b) -> bool {
-    const int w = tid + k * kThreads;
-    if (w >= npairs) return false;
-    i = w / p.topk;
-    b = sel[k];
-    const int pos = ctl.tok_pos[i];
-    return pos >= 0 && b >= 0 && b < p.nblocks && b * kBlk <= pos &&
-           b * kBlk + kBlk - 1 >= ctl.tok_lo[i];
-  };
-#pragma unroll
-  for (int k = 0; k < kPairsPerThread; ++k) {
-    int i, b;
-    if (live_block(k, i, b)) atomicOr(&ctl.bitmap[b >> 5], 1u << (b & 31));
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // exclusive prefix of popcounts over the bitmap words
-    const int per = (nwords + 31) >> 5;
-    int local = 0;
-    for (int k = 0; k < per; ++k) {
-      const int w = lane * per + k;
-      if (w < nwords) local += __popc(ctl.bitmap[w]);
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - local;
-    for (int k = 0; k < per; ++k) {
-      const int w = lane * per + k;
-      if (w < nwords) {
-        ctl.prefix[w] = run;
-        run += __popc(ctl.bitmap[w]);
-      }
-    }
-    if (lane == 31) ctl.nunion = incl;
-  }
-  __syncthreads();
-  const int U = ctl.nunion;
-  for (int w = tid; w < nwords; w += kThreads) {
-    uint32_t bits = ctl.bitmap[w];
-    int o = ctl.prefix[w];
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1;
-      ulist[o++] = w * 32 + b;
-    }
-  }
-  for (int w = tid; w < U * TW; w += kThreads) tokmask[w] = 0u;
-  __syncthreads();
-#pragma unroll
-  for (int k = 0; k < kPairsPerThread; ++k) {
-    int i, b;
-    if (live_block(k, i, b)) {
-      const uint32_t word = ctl.bitmap[b >> 5];
-      const int u = ctl.prefix[b >> 5] + __popc(word & ((1u << (b & 31)) - 1u));
-      atomicOr(&tokmask[u * TW + (i >> 5)], 1u << (i & 31));
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
-  const int nsteps = (U + 1) >> 1;
-  bool ok = true;
-
-  // K and V of step j stream through separate rings with their own producer
-  // threads: K (needed first, by S) runs KST steps ahead of the MMAs, V (needed
-  // after the softmax) two.
-  auto produce = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* empty,
-                     int nst) {
-    int issued = 0;
-    bool pok = true;
-    for (int j = 0; j < nsteps; ++j) {
-      const int st = j % nst;
-      if (j >= nst) {
-        pok = mbar_wait(&empty[st], ((j / nst) - 1) & 1, p.err, kErrWaitFree);
-        if (!pok) break;
-      }
-      const int nb = min(2, U - 2 * j);
-      uint8_t* stage = ring + st * kStepBytes;
-      mbar_arrive_expect_tx(&full[st], (uint32_t)nb * 2u * (kBlk * 128));
-      for (int bi = 0; bi < nb; ++bi) {
-        const int kpos = row_start + ulist[2 * j + bi] * kBlk;
-        for (int s = 0; s < 2; ++s)
-          tma_load_3d(stage + s * kKVSlab + bi * (kBlk * 128), map, &full[st], 64 * s, g, kpos);
-      }
-      issued = j + 1;
-    }
-    if (!pok) {
-      // bounded drain of the copies still in flight
-      for (int j = max(0, issued - nst); j < issued; ++j)
-        mbar_wait(&full[j % nst], (j / nst) & 1, p.err, kErrWaitDrain);
-    }
+  volatile int32_t* abort_flag = &ctl.abort_flag;
+  // A bounded wait that ran out stops every role: each checks the flag
+  // before its next wait, so a failure costs at most one more time-out per
+  // role instead of one per remaining step.
+  auto wait_or_abort = [&](uint64_t* bar, uint32_t parity, uint32_t site) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity, p.err, site)) return true;
+    *abort_flag = 1;
+    return false;
   };
-  if (tid == 0 && nsteps > 0) {
-    // ---- K producer (Q was loaded during the set-up) --------------------------
-    produce(&tm_k, sK, ctl.k_full, ctl.k_empty, KST);
-  } else if (tid == 96 && nsteps > 0) {
-    // ---- V producer ------------------------------------------------------------
-    produce(&tm_v, sV, ctl.v_full, ctl.v_empty, kVStages);
-  } else if (tid == 32 && nsteps > 0) {
-    // ---- MMA issuer ----------------------------------------------------------
-    ok = mbar_wait(&ctl.q_full, 0, p.err, kErrWaitLoad);
-    auto issue_s = [&](int j) -> bool {
-      const int st = j & 1;  // S buffer
-      const int ks = j % KST;
-      if (!mbar_wait(&ctl.k_full[ks], (j / KST) & 1, p.err, kErrWaitLoad)) return false;
-      tc_fence_after();
-      const int nb = min(2, U - 2 * j);
-      const uint32_t idesc = idesc_bf16(128, nb * kBlk, false);
-      const uint8_t* kst = sK + ks * kStepBytes;
-#pragma unroll
-      for (int s = 0; s < 2; ++s) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = smem_desc(smem_u32(sQ + s * kQSlab) + kk * 32, 16, 1024, kLayoutSw128);
-          const uint64_t b = smem_desc(smem_u32(kst + s * kKVSlab) + kk * 32, 16, 1024, kLayoutSw128);
-          mma_ss(tmem + (uint32_t)(st * 128), a, b, idesc, (s | kk) ? 1u : 0u);
+
+  if (warp == 2) {
+    // ---- metadata of each tile (one warp), a tile ahead of the others --------
+    for (int n = 0; n < nmine; ++n) {
+      const int tb = n & 1;
+      if (n >= 2 && !wait_or_abort(&ctl.meta_empty[tb], ((n >> 1) - 1) & 1, kErrWaitFree)) break;
+      int g, tok0;
+      tile_of(n, g, tok0);
+      const int row_start = (tok0 / p.seq_len) * p.seq_len;
+      int32_t* tpos = ctl.tok_pos[tb];
+      int32_t* tlo = ctl.tok_lo[tb];
+      for (int i = lane; i < TQ; i += 32) {
+        const int t = tok0 + i;
+        if (t < p.total_tokens) {
+          const int doc = upper_doc(p.cu_docs, p.num_docs, t);
+          tpos[i] = t - row_start;
+          tlo[i] = max(doc - row_start, 0);
+          ctl.tok_k0[tb][i] = doc >= row_start ? doc - row_start : -1;
+        } else {
+          tpos[i] = -1;
+          tlo[i] = 0;
+          ctl.tok_k0[tb][i] = -1;
         }
       }
-      mma_commit(&ctl.k_empty[ks]);
-      mma_commit(&ctl.s_full[st]);
-      return true;
-    };
-    if (ok) ok = issue_s(0);
-    for (int j = 0; j < nsteps && ok; ++j) {
-      if (j + 1 < nsteps) {
-        ok = issue_s(j + 1);
+      for (int w = lane; w < nwords; w += 32) ctl.bitmap[w] = 0u;
+      __syncwarp();
+      // the selection of this KV head's index head, rows of the tile's tokens
+      const int32_t* table = p.table + (int64_t)(g / p.kv_per_index_head) * p.table_head_stride +
+                             (int64_t)tok0 * p.topk;
+      const int npairs = TQ * p.topk;
+      // pair w = (token i, entry): its block b is live when it intersects
+      // [document start, position]
+      auto live_block = [&](int w, int& i, int& b) -> bool {
+        i = w / p.topk;
+        b = __ldg(table + w);
+        const int pos = tpos[i];
+        return pos >= 0 && b >= 0 && b < p.nblocks && b * kBlk <= pos &&
+               b * kBlk + kBlk - 1 >= tlo[i];
+      };
+      for (int w = lane; w < npairs; w += 32) {
+        int i, b;
+        if (live_block(w, i, b)) atomicOr(&ctl.bitmap[b >> 5], 1u << (b & 31));
+      }
+      __syncwarp();
+      {
+        // exclusive prefix of popcounts over the bitmap words
+        const int per = (nwords + 31) >> 5;
+        int local = 0;
+        for (int k = 0; k < per; ++k) {
+          const int w = lane * per + k;
+          if (w < nwords) local += __popc(ctl.bitmap[w]);
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int k = 0; k < per; ++k) {
+          const int w = lane * per + k;
+          if (w < nwords) {
+            ctl.prefix[w] = run;
+            run += __popc(ctl.bitmap[w]);
+          }
+        }
+        if (lane == 31) ctl.nunion[tb] = incl;
+      }
+      __syncwarp();
+      const int U = ctl.nunion[tb];
+      int32_t* ulist = ulist2 + tb * kMaxUnion;
+      uint32_t* tokmask = tokmask2 + tb * kMaxUnion * TW;
+      for (int w = lane; w < nwords; w += 32) {
+        uint32_t bits = ctl.bitmap[w];
+        int o = ctl.prefix[w];
+        while (bits) {
+          const int b = __ffs(bits) - 1;
+          bits &= bits - 1;
+          ulist[o++] = w * 32 + b;
+        }
+      }
+      for (int w = lane; w < U * TW; w += 32) tokmask[w] = 0u;
+      __syncwarp();
+      for (int w = lane; w < npairs; w += 32) {
+        int i, b;
+        if (live_block(w, i, b)) {
+          const uint32_t word = ctl.bitmap[b >> 5];
+          const int u = ctl.prefix[b >> 5] + __popc(word & ((1u << (b & 31)) - 1u));
+          atomicOr(&tokmask[u * TW + (i >> 5)], 1u << (i & 31));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.meta_full[tb]);
+    }
+  } else if (tid == 0) {
+    // ---- K producer: runs KST steps ahead of S, across tile boundaries -------
+    int gk = 0, issued = 0;
+    for (int n = 0; n < nmine; ++n) {
+      const int tb = n & 1;
+      if (!wait_or_abort(&ctl.meta_full[tb], (n >> 1) & 1, kErrWaitLoad)) break;
+      int g, tok0;
+      tile_of(n, g, tok0);
+      const int row_start = (tok0 / p.seq_len) * p.seq_len;
+      const int U = ctl.nunion[tb];
+      const int32_t* ulist = ulist2 + tb * kMaxUnion;
+      bool pok = true;
+      for (int j = 0; 2 * j < U; ++j, ++gk) {
+        const int st = gk % KST;
+        if (gk >= KST && !(pok = wait_or_abort(&ctl.k_empty[st], ((gk / KST) - 1) & 1, kErrWaitFree)))
+          break;
+        const int nb = min(2, U - 2 * j);
+        uint8_t* stage = sK + st * kStepBytes;
+        mbar_arrive_expect_tx(&ctl.k_full[st], (uint32_t)nb * 2u * (kBlk * 128));
+        for (int bi = 0; bi < nb; ++bi) {
+          const int kpos = row_start + ulist[2 * j + bi] * kBlk;
+          for (int s = 0; s < 2; ++s)
+            tma_load_3d(stage + s * kKVSlab + bi * (kBlk * 128), &tm_k, &ctl.k_full[st], 64 * s,
+                        g, kpos);
+        }
+        issued = gk + 1;
+      }
+      mbar_arrive(&ctl.meta_empty[tb]);
+      if (!pok) break;
+    }
+    if (*abort_flag) {
+      // bounded drain of the copies still in flight
+      for (int q = max(0, issued - KST); q < issued; ++q)
+        mbar_wait(&ctl.k_full[q % KST], (q / KST) & 1, p.err, kErrWaitDrain);
+    }
+  } else if (tid == 96) {
+    // ---- Q and V producer: Q of a tile once the previous tile's last S has
+    // read Q, then V two steps ahead of P V ----------------------------------
+    int gv = 0, issued = 0, nq = 0;
+    for (int n = 0; n < nmine; ++n) {
+      const int tb = n & 1;
+      if (!wait_or_abort(&ctl.meta_full[tb], (n >> 1) & 1, kErrWaitLoad)) break;
+      int g, tok0;
+      tile_of(n, g, tok0);
+      const int row_start = (tok0 / p.seq_len) * p.seq_len;
+      const int U = ctl.nunion[tb];
+      const int32_t* ulist = ulist2 + tb * kMaxUnion;
+      if (n >= 1 && !wait_or_abort(&ctl.q_empty, (n - 1) & 1, kErrWaitFree)) {
+        mbar_arrive(&ctl.meta_empty[tb]);
+        break;
+      }
+      mbar_arrive_expect_tx(&ctl.q_full, 2 * kQSlab);
+      for (int s2 = 0; s2 < 2; ++s2)
+        tma_load_3d(sQ + s2 * kQSlab, &tm_q, &ctl.q_full, 64 * s2, g * G, tok0);
+      nq = n + 1;
+      bool pok = true;
+      for (int j = 0; 2 * j < U; ++j, ++gv) {
+        const int st = gv % kVStages;
+        if (gv >= kVStages &&
+            !(pok = wait_or_abort(&ctl.v_empty[st], ((gv / kVStages) - 1) & 1, kErrWaitFree)))
+          break;
+        const int nb = min(2, U - 2 * j);
+        uint8_t* stage = sV + st * kStepBytes;
+        mbar_arrive_expect_tx(&ctl.v_full[st], (uint32_t)nb * 2u * (kBlk * 128));
+        for (int bi = 0; bi < nb; ++bi) {
+          const int kpos = row_start + ulist[2 * j + bi] * kBlk;
+          for (int s = 0; s < 2; ++s)
+            tma_load_3d(stage + s * kKVSlab + bi * (kBlk * 128), &tm_v, &ctl.v_full[st], 64 * s,
+                        g, kpos);
+        }
+        issued = gv + 1;
+      }
+      mbar_arrive(&ctl.meta_empty[tb]);
+      if (!pok) break;
+    }
+    if (*abort_flag) {
+      for (int q = max(0, issued - kVStages); q < issued; ++q)
+        mbar_wait(&ctl.v_full[q % kVStages], (q / kVStages) & 1, p.err, kErrWaitDrain);
+      if (nq > 0) mbar_wait(&ctl.q_full, (nq - 1) & 1, p.err, kErrWaitDrain);
+    }
+  } else if (tid == 32) {
+    // ---- MMA issuer ----------------------------------------------------------
+    int gs = 0;  // steps of earlier tiles: S / P buffers and o_done phases
+    for (int n = 0; n < nmine; ++n) {
+      const int tb = n & 1;
+      if (!wait_or_abort(&ctl.meta_full[tb], (n >> 1) & 1, kErrWaitLoad)) break;
+      const int U = ctl.nunion[tb];
+      const int nsteps = (U + 1) >> 1;
+      bool ok = wait_or_abort(&ctl.q_full, n & 1, kErrWaitLoad);
+      if (ok && nsteps == 0) mbar_arrive(&ctl.q_empty);  // Q unused: release it
+      auto issue_s = [&](int j) -> bool {
+        const int gj = gs + j;
+        const int st = gj & 1;  // S buffer
+        const int ks = gj % KST;
+        if (!wait_or_abort(&ctl.k_full[ks], (gj / KST) & 1, kErrWaitLoad)) return false;
+        tc_fence_after();
+        const int nb = min(2, U - 2 * j);
+        const uint32_t idesc = idesc_bf16(128, nb * kBlk, false);
+        const uint8_t* kst = sK + ks * kStepBytes;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = smem_desc(smem_u32(sQ + s * kQSlab) + kk * 32, 16, 1024, kLayoutSw128);
+            const uint64_t b = smem_desc(smem_u32(kst + s * kKVSlab) + kk * 32, 16, 1024, kLayoutSw128);
+            mma_ss(tmem + (uint32_t)(st * 128), a, b, idesc, (s | kk) ? 1u : 0u);
+          }
+        }
+        mma_commit(&ctl.k_empty[ks]);
+        if (j == nsteps - 1) mma_commit(&ctl.q_empty);  // the tile's last read of Q
+        mma_commit(&ctl.s_full[st]);
+        return true;
+      };
+      if (ok && nsteps > 0) ok = issue_s(0);
+      for (int j = 0; j < nsteps && ok; ++j) {
+        if (j + 1 < nsteps) {
+          ok = issue_s(j + 1);
+          if (!ok) break;
+        }
+        const int gj = gs + j;
+        const int st = gj & 1;
+        ok = wait_or_abort(&ctl.p_full[st], (gj >> 1) & 1, kErrWaitMma);
         if (!ok) break;
+        // the first P V of a tile overwrites O: the previous epilogue must have read it
+        if (j == 0 && n > 0) {
+          ok = wait_or_abort(&ctl.o_free, (n - 1) & 1, kErrWaitFree);
+          if (!ok) break;
+        }
+        const int vs = gj % kVStages;
+        ok = wait_or_abort(&ctl.v_full[vs], (gj / kVStages) & 1, kErrWaitLoad);
+        if (!ok) break;
+        tc_fence_after();
+        const int nb = min(2, U - 2 * j);
+        const uint32_t idesc = idesc_bf16(128, kD, true);
+        const uint8_t* vst = sV + vs * kStepBytes;
+        for (int kk = 0; kk < nb * kBlk / 16; ++kk) {
+          const uint64_t b = smem_desc(smem_u32(vst) + kk * 16 * 128, kKVSlab, 1024, kLayoutSw128);
+          // P of block kk / 4 sits in the first half of that block's S columns
+          mma_ts(tmem + kColO, tmem + (uint32_t)(st * 128 + 64 * (kk >> 2) + 8 * (kk & 3)), b,
+                 idesc, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&ctl.v_empty[vs]);
+        mma_commit(&ctl.o_done);
       }
-      const int st = j & 1;
-      ok = mbar_wait(&ctl.p_full[st], (j >> 1) & 1, p.err, kErrWaitMma);
+      mbar_arrive(&ctl.meta_empty[tb]);
       if (!ok) break;
-      tc_fence_after();
-      ok = mbar_wait(&ctl.v_full[st], (j >> 1) & 1, p.err, kErrWaitLoad);
-      if (!ok) break;
-      tc_fence_after();
-      const int nb = min(2, U - 2 * j);
-      const uint32_t idesc = idesc_bf16(128, kD, true);
-      const uint8_t* vst = sV + st * kStepBytes;
-      for (int kk = 0; kk < nb * kBlk / 16; ++kk) {
-        const uint64_t b = smem_desc(smem_u32(vst) + kk * 16 * 128, kKVSlab, 1024, kLayoutSw128);
-        // P of block kk / 4 sits in the first half of that block's S columns
-        mma_ts(tmem + kColO, tmem + (uint32_t)(st * 128 + 64 * (kk >> 2) + 8 * (kk & 3)), b, idesc,
-               (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      mma_commit(&ctl.v_empty[st]);
-      mma_commit(&ctl.o_done);
+      gs += nsteps;
     }
   } else if (warp >= 4) {
     // ---- softmax + epilogue -------------------------------------------------
@@ -390,188 +477,229 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int part = (warp - 4) >> 2;
     const int row = (warp & 3) * 32 + lane;
     const int tok = row / G;
-    const int h = g * G + (row % G);
-    const int t = tok0 + tok;
-    const int pos = ctl.tok_pos[tok];
-    const int dlo = ctl.tok_lo[tok];
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const float c2 = p.scale_log2;
-    const float k0_sink2 = (MODE == SA_SINK_KEY0_BIAS) ? __ldg(p.sinks + h) * kLog2e : 0.f;
-    float m_use = -INFINITY, l = 0.f;
+    int gs = 0, cp = 0;
+    // The eight warps share named barrier 1, which has no time limit, so they
+    // stop together or not at all: a failure is posted before a barrier and
+    // every thread reads the decision right after it (the slot alternates, so
+    // a later post cannot race a late reader).
+    auto checkpoint = [&](bool fail) -> bool {
+      if (fail) ctl.sm_stop[cp & 1] = 1;
+      if (warp == 4 && lane == 0 && *abort_flag) ctl.sm_stop[cp & 1] = 1;
+      bar_softmax();
+      const bool stop = ctl.sm_stop[cp & 1] != 0;
+      ++cp;
+      return stop;
+    };
+    for (int n = 0; n < nmine; ++n) {
+      const int tb = n & 1;
+      const bool meta_ok = wait_or_abort(&ctl.meta_full[tb], (n >> 1) & 1, kErrWaitLoad);
+      if (checkpoint(!meta_ok)) break;
+      bool ok = true;
+      int g, tok0;
+      tile_of(n, g, tok0);
+      const int h = g * G + (row % G);
+      const int t = tok0 + tok;
+      const int pos = ctl.tok_pos[tb][tok];
+      const int dlo = ctl.tok_lo[tb][tok];
+      const int k0 = ctl.tok_k0[tb][tok];
+      const int U = ctl.nunion[tb];
+      const int nsteps = (U + 1) >> 1;
+      const int32_t* ulist = ulist2 + tb * kMaxUnion;
+      const uint32_t* tokmask = tokmask2 + tb * kMaxUnion * TW;
+      const float k0_sink2 = (MODE == SA_SINK_KEY0_BIAS) ? __ldg(p.sinks + h) * kLog2e : 0.f;
+      float m_use = -INFINITY, l = 0.f;
 
-    for (int j = 0; j < nsteps; ++j) {
-      const int st = j & 1;
-      ok = mbar_wait(&ctl.s_full[st], (j >> 1) & 1, p.err, kErrWaitMma) && ok;
-      __syncwarp();
-      tc_fence_after();
-      // live columns of this thread's block: [clo, chi] within the block
-      const int u = 2 * j + part;
-      int clo = 1 << 30, chi = 1 << 30;
-      int k0c = -1;  // KEY0_BIAS: column of the document's first key in this block
-      if (u < U && pos >= 0 && ((tokmask[u * TW + (tok >> 5)] >> (tok & 31)) & 1u)) {
-        const int bs = ulist[u] * kBlk;
-        clo = max(dlo, bs) - bs;
-        chi = min(pos, bs + kBlk - 1) - bs;
-        if (MODE == SA_SINK_KEY0_BIAS) {
-          const int k0 = ctl.tok_k0[tok];
-          if (k0 >= bs && k0 < bs + kBlk) k0c = k0 - bs;  // then k0c == clo: live
+      for (int j = 0; j < nsteps; ++j) {
+        const int gj = gs + j;
+        const int st = gj & 1;
+        ok = wait_or_abort(&ctl.s_full[st], (gj >> 1) & 1, kErrWaitMma) && ok;
+        __syncwarp();
+        tc_fence_after();
+        // live columns of this thread's block: [clo, chi] within the block
+        const int u = 2 * j + part;
+        int clo = 1 << 30, chi = 1 << 30;
+        int k0c = -1;  // KEY0_BIAS: column of the document's first key in this block
+        if (u < U && pos >= 0 && ((tokmask[u * TW + (tok >> 5)] >> (tok & 31)) & 1u)) {
+          const int bs = ulist[u] * kBlk;
+          clo = max(dlo, bs) - bs;
+          chi = min(pos, bs + kBlk - 1) - bs;
+          if (MODE == SA_SINK_KEY0_BIAS) {
+            if (k0 >= bs && k0 < bs + kBlk) k0c = k0 - bs;  // then k0c == clo: live
+          }
         }
-      }
-      const bool has_k0 = MODE == SA_SINK_KEY0_BIAS && __any_sync(0xffffffffu, k0c >= 0);
-      const uint32_t span = (uint32_t)(chi - clo);
-      const bool warp_live = __any_sync(0xffffffffu, clo != (1 << 30));
-      const uint32_t sbase = lane_base + (uint32_t)(st * 128 + 64 * part);
-      float s[2][32];
-      float mx = -INFINITY;
-      float sk0 = -INFINITY;  // raw logit of the KEY0_BIAS key (taken out of s)
-      if (warp_live) {
-        tmem_ld32(sbase, s[0]);
-        tmem_ld32(sbase + 32, s[1]);
-        tmem_wait_ld();
-        float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (has_k0) {
+        const bool has_k0 = MODE == SA_SINK_KEY0_BIAS && __any_sync(0xffffffffu, k0c >= 0);
+        const uint32_t span = (uint32_t)(chi - clo);
+        const bool warp_live = __any_sync(0xffffffffu, clo != (1 << 30));
+        const uint32_t sbase = lane_base + (uint32_t)(st * 128 + 64 * part);
+        float s[2][32];
+        float mx = -INFINITY;
+        float sk0 = -INFINITY;  // raw logit of the KEY0_BIAS key (taken out of s)
+        if (warp_live) {
+          tmem_ld32(sbase, s[0]);
+          tmem_ld32(sbase + 32, s[1]);
+          tmem_wait_ld();
+          float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (has_k0) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                sk0 = (32 * c + e == k0c) ? s[c][e] : sk0;
+                s[c][e] = ((uint32_t)(32 * c + e - clo) <= span && 32 * c + e != k0c) ? s[c][e]
+                                                                                      : -INFINITY;
+              }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                s[c][e] = ((uint32_t)(32 * c + e - clo) <= span) ? s[c][e] : -INFINITY;
+          }
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              sk0 = (32 * c + e == k0c) ? s[c][e] : sk0;
-              s[c][e] = ((uint32_t)(32 * c + e - clo) <= span && 32 * c + e != k0c) ? s[c][e]
-                                                                                    : -INFINITY;
+            for (int e = 0; e < 32; e += 2)
+              mr[(e >> 1) & 3] = max3f(mr[(e >> 1) & 3], s[c][e], s[c][e + 1]);
+          // max(s) * c2 == max(s * c2) exactly; the biased key enters scaled
+          mx = fmaxf(fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * c2, sk0 * c2 + k0_sink2);
+        }
+        ctl.red_m[st][part][row] = mx;
+        bar_softmax();
+        mx = fmaxf(ctl.red_m[st][0][row], ctl.red_m[st][1][row]);
+        // lazy rescale of O and l when this row's max grew by more than 2^8
+        const bool need = mx > m_use + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mx : m_use;
+          const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
+          if (j > 0) {
+            ok = wait_or_abort(&ctl.o_done, (gj - 1) & 1, kErrWaitMma) && ok;
+            __syncwarp();
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+              float o[32];
+              const uint32_t oa = lane_base + kColO + 64 * part + 32 * c;
+              tmem_ld32(oa, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= alpha;
+              tmem_st32(oa, o);
             }
+            tmem_wait_st();
+            l *= alpha;
+          }
+          m_use = m_new;
+        }
+        if (warp_live) {
+          // P = 2^(x - m) (bf16) into the first 32 columns of this block's S
+          // region, behind this thread's own reads; masked columns give 0
+          const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;
+          const uint64_t c2c2 = f2_pack(c2, c2), nmnm = f2_pack(-m_ref, -m_ref);
+          // the biased key's exponent: fma(s, c2, -m) + sink (bitwise the no-sink
+          // value for a zero sink)
+          const float xk0 = fmaf(sk0, c2, -m_ref) + k0_sink2;
+          uint64_t lp[4] = {0, 0, 0, 0};
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const uint64_t x = f2_fma(f2_pack(s[c][e], s[c][e + 1]), c2c2, nmnm);
+              float x0 = f2_lo(x), x1 = f2_hi(x);
+              if (has_k0) {
+                x0 = (32 * c + e == k0c) ? xk0 : x0;
+                x1 = (32 * c + e + 1 == k0c) ? xk0 : x1;
+              }
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              lp[(e >> 1) & 3] = f2_add(lp[(e >> 1) & 3], f2_pack(p0, p1));
+              pk[e >> 1] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(sbase + 16 * c, pk);
+          }
+          const uint64_t ls = f2_add(f2_add(lp[0], lp[1]), f2_add(lp[2], lp[3]));
+          l += f2_lo(ls) + f2_hi(ls);
+        } else if (u < U) {
+          // block present for the tile but not for these rows: P = 0
+          uint32_t z[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) z[e] = 0u;
+          tmem_st16(sbase, z);
+          tmem_st16(sbase + 16, z);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.p_full[st]);
+      }
+      if (nsteps > 0) {
+        // O is final once the last P V is done.  A parity wait only tells a
+        // phase from the one before it, and here o_done may still be two
+        // phases short (P V(last - 1) is issued after S(last), whose
+        // completion is all this thread has seen), so wait for the two phases
+        // in turn.
+        if (nsteps > 1)
+          ok = wait_or_abort(&ctl.o_done, (gs + nsteps - 2) & 1, kErrWaitMma) && ok;
+        ok = wait_or_abort(&ctl.o_done, (gs + nsteps - 1) & 1, kErrWaitMma) && ok;
+        __syncwarp();
+        tc_fence_after();
+      }
+      ctl.red_l[tb][part][row] = l;
+      const bool stop = checkpoint(!ok);  // (also the barrier of the row-sum exchange)
+      const float lt = ctl.red_l[tb][0][row] + ctl.red_l[tb][1][row];
+      // epilogue: this thread stores O columns [64 part, 64 part + 64)
+      float inv = 0.f, lse = -INFINITY;
+      if (m_use != -INFINITY) {
+        float den = lt, alpha = 1.f;
+        if (MODE == SA_SINK_NULL_LOGIT) {
+          const float sink2 = __ldg(p.sinks + h) * kLog2e;
+          const float mp = fmaxf(m_use, sink2);
+          alpha = ex2_approx(m_use - mp);
+          den = lt * alpha + ex2_approx(sink2 - mp);
+        }
+        inv = alpha / den;
+        lse = (m_use + log2f(lt)) * kLn2;
+      }
+      const bool row_valid = pos >= 0;
+      __nv_bfloat16* orow = p.out + ((int64_t)t * p.num_q_heads + h) * kD + 64 * part;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        float o[32];
+        if (nsteps > 0) {
+          tmem_ld32(lane_base + kColO + 64 * part + 32 * c, o);
+          tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              s[c][e] = ((uint32_t)(32 * c + e - clo) <= span) ? s[c][e] : -INFINITY;
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
         }
+        if (row_valid) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mr[(e >> 1) & 3] = max3f(mr[(e >> 1) & 3], s[c][e], s[c][e + 1]);
-        // max(s) * c2 == max(s * c2) exactly; the biased key enters scaled
-        mx = fmaxf(fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * c2, sk0 * c2 + k0_sink2);
-      }
-      ctl.red_m[st][part][row] = mx;
-      bar_softmax();
-      mx = fmaxf(ctl.red_m[st][0][row], ctl.red_m[st][1][row]);
-      // lazy rescale of O and l when this row's max grew by more than 2^8
-      const bool need = mx > m_use + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? mx : m_use;
-        const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
-        if (j > 0) {
-          ok = mbar_wait(&ctl.o_done, (j - 1) & 1, p.err, kErrWaitMma) && ok;
-          __syncwarp();
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            float o[32];
-            const uint32_t oa = lane_base + kColO + 64 * part + 32 * c;
-            tmem_ld32(oa, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(oa, o);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16x2(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
+            w.y = pack_bf16x2(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
+            w.z = pack_bf16x2(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
+            w.w = pack_bf16x2(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * q4) = w;
           }
-          tmem_wait_st();
-          l *= alpha;
         }
-        m_use = m_new;
       }
-      if (warp_live) {
-        // P = 2^(x - m) (bf16) into the first 32 columns of this block's S
-        // region, behind this thread's own reads; masked columns give 0
-        const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;
-        const uint64_t c2c2 = f2_pack(c2, c2), nmnm = f2_pack(-m_ref, -m_ref);
-        // the biased key's exponent: fma(s, c2, -m) + sink (bitwise the no-sink
-        // value for a zero sink)
-        const float xk0 = fmaf(sk0, c2, -m_ref) + k0_sink2;
-        uint64_t lp[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const uint64_t x = f2_fma(f2_pack(s[c][e], s[c][e + 1]), c2c2, nmnm);
-            float x0 = f2_lo(x), x1 = f2_hi(x);
-            if (has_k0) {
-              x0 = (32 * c + e == k0c) ? xk0 : x0;
-              x1 = (32 * c + e + 1 == k0c) ? xk0 : x1;
-            }
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            lp[(e >> 1) & 3] = f2_add(lp[(e >> 1) & 3], f2_pack(p0, p1));
-            pk[e >> 1] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(sbase + 16 * c, pk);
-        }
-        const uint64_t ls = f2_add(f2_add(lp[0], lp[1]), f2_add(lp[2], lp[3]));
-        l += f2_lo(ls) + f2_hi(ls);
-      } else if (u < U) {
-        // block present for the tile but not for these rows: P = 0
-        uint32_t z[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) z[e] = 0u;
-        tmem_st16(sbase, z);
-        tmem_st16(sbase + 16, z);
-      }
-      tmem_wait_st();
+      // O has been read: the next tile's first P V may overwrite it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.p_full[st]);
-    }
-    if (nsteps > 0) {
-      ok = mbar_wait(&ctl.o_done, (nsteps - 1) & 1, p.err, kErrWaitMma) && ok;
-      __syncwarp();
-      tc_fence_after();
-    }
-    ctl.red_l[part][row] = l;
-    bar_softmax();
-    const float lt = ctl.red_l[0][row] + ctl.red_l[1][row];
-    // epilogue: this thread stores O columns [64 part, 64 part + 64)
-    float inv = 0.f, lse = -INFINITY;
-    if (m_use != -INFINITY) {
-      float den = lt, alpha = 1.f;
-      if (MODE == SA_SINK_NULL_LOGIT) {
-        const float sink2 = __ldg(p.sinks + h) * kLog2e;
-        const float mp = fmaxf(m_use, sink2);
-        alpha = ex2_approx(m_use - mp);
-        den = lt * alpha + ex2_approx(sink2 - mp);
+      if (lane == 0) mbar_arrive(&ctl.o_free);
+      if (row_valid && part == 0) p.lse[(int64_t)h * p.total_tokens + t] = lse;
+      if (lane == 0) mbar_arrive(&ctl.meta_empty[tb]);
+      if (stop) {
+        *abort_flag = 1;
+        break;
       }
-      inv = alpha / den;
-      lse = (m_use + log2f(lt)) * kLn2;
+      gs += nsteps;
     }
-    const bool row_valid = pos >= 0;
-    __nv_bfloat16* orow = p.out + ((int64_t)t * p.num_q_heads + h) * kD + 64 * part;
-#pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      float o[32];
-      if (nsteps > 0) {
-        tmem_ld32(lane_base + kColO + 64 * part + 32 * c, o);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0.f;
-      }
-      if (row_valid) {
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 w;
-          w.x = pack_bf16x2(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
-          w.y = pack_bf16x2(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
-          w.z = pack_bf16x2(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
-          w.w = pack_bf16x2(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
-          *reinterpret_cast<uint4*>(orow + 32 * c + 8 * q4) = w;
-        }
-      }
-    }
-    if (row_valid && part == 0) p.lse[(int64_t)h * p.total_tokens + t] = lse;
   }
 
   // ---- teardown ----------------------------------------------------------------
-  // a tile without live blocks never consumed its Q copy: let it land first
-  if (tid == 0 && nsteps == 0) mbar_wait(&ctl.q_full, 0, p.err, kErrWaitDrain);
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
@@ -611,6 +739,7 @@ sa_status launch_typed(const BlockArgs& a) {
   p.cu_docs = a.cu_docs;
   p.num_docs = a.num_docs;
   p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
   p.sinks = a.sinks;
   p.scale_log2 = a.softmax_scale * kLog2e;
   p.out = reinterpret_cast<__nv_bfloat16*>(a.out);
@@ -621,7 +750,10 @@ sa_status launch_typed(const BlockArgs& a) {
   if (!set_dynamic_smem_once((const void*)kern, (int)smem))
     return fail(SA_ERR_CUDA, "sa_block_sparse_fwd: %s", cudaGetErrorString(cudaGetLastError()));
   cudaError_t e;
-  dim3 grid((unsigned)(T / TQ), (unsigned)a.num_kv_heads);
+  // persistent: one CTA per SM (the shared memory allows one), each walking
+  // tiles blockIdx.x, blockIdx.x + grid, ...
+  const int64_t ntiles = (T / TQ) * a.num_kv_heads;
+  const unsigned grid = (unsigned)std::min<int64_t>(ntiles, num_sms());
   kern<<<grid, kThreads, smem, a.stream>>>(tq, tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess)
@@ -653,10 +785,12 @@ sa_status launch_block_sparse_fwd(const BlockArgs& a) {
   if (a.seq_len / kBlk > kMaxBitmapWords * 32)
     return fail(SA_ERR_UNSUPPORTED, "%s: seq_len %d above %d", fn, a.seq_len,
                 kMaxBitmapWords * 32 * kBlk);
-  if ((128 / G) * a.topk_blocks > kMaxUnion)
+  // blocks in a tile's union: at most its selections and at most the row's blocks
+  if (std::min<int64_t>((int64_t)(128 / G) * a.topk_blocks, a.seq_len / kBlk) > kMaxUnion)
     return fail(SA_ERR_UNSUPPORTED,
-                "%s: %d tokens per tile x topk_blocks %d above %d selections per tile", fn,
-                128 / G, a.topk_blocks, kMaxUnion);
+                "%s: %d tokens per tile x topk_blocks %d (and %d blocks per row) above %d "
+                "union blocks per tile",
+                fn, 128 / G, a.topk_blocks, a.seq_len / kBlk, kMaxUnion);
   switch (G) {
     case 1: return by_mode<1>(a);
     case 2: return by_mode<2>(a);
