@@ -46,7 +46,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kD = 128;
 constexpr int kBlk = 64;
 constexpr int kStepKeys = 128;                 // two blocks per step
-constexpr int kMaxKStages = 3;                 // K ring (fewer where shared memory is short)
+constexpr int kKStages = 2;                    // K ring
 constexpr int kVStages = 2;                    // V ring
 constexpr int kQSlab = 128 * 128;              // 128 rows x 64 dims, 16 KB
 constexpr int kKVSlab = kStepKeys * 128;       // 128 keys x 64 dims, 16 KB
@@ -79,8 +79,8 @@ struct BlockParams {
 
 struct __align__(8) BlockSmemCtl {
   uint64_t q_full, q_empty;
-  uint64_t k_full[kMaxKStages];
-  uint64_t k_empty[kMaxKStages];
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];
   uint64_t s_full[2];
@@ -139,15 +139,15 @@ __device__ __forceinline__ int upper_doc(const int32_t* cu, int n, int t) {
   return __ldg(cu + lo);
 }
 
-// Dynamic shared memory with KST K stages: Q, the K and V rings, and two
-// metadata buffers (union list and its token masks).
-__host__ __device__ constexpr size_t block_smem_bytes(int G, int KST) {
-  return 1024 + 2 * (size_t)kQSlab + (size_t)KST * kStepBytes + (size_t)kVStages * kStepBytes +
+// Dynamic shared memory: Q, the K and V rings, and two metadata buffers
+// (union list and its token masks).  (Measured: a third K stage, or a second
+// Q buffer with the next tile's first S issued early, made the persistent
+// kernel slower; the shared memory they take comes out of the L1 cache.)
+__host__ __device__ constexpr size_t block_smem_bytes(int G) {
+  return 1024 + 2 * (size_t)kQSlab + (size_t)kKStages * kStepBytes +
+         (size_t)kVStages * kStepBytes +
          2 * ((size_t)kMaxUnion * 4 +
               (size_t)kMaxUnion * ((128 / G) > 32 ? (128 / G) / 32 : 1) * 4);
-}
-__host__ __device__ constexpr int block_k_stages(int G) {
-  return block_smem_bytes(G, 3) + sizeof(BlockSmemCtl) <= 227 * 1024 ? 3 : 2;
 }
 
 template <int G, int MODE>
@@ -158,7 +158,7 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const BlockParams p) {
   constexpr int TQ = 128 / G;
   constexpr int TW = TQ > 32 ? TQ / 32 : 1;  // token-mask words per block
-  constexpr int KST = block_k_stages(G);
+  constexpr int KST = kKStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ BlockSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -711,8 +711,7 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 template <int G, int MODE>
 sa_status launch_typed(const BlockArgs& a) {
   constexpr int TQ = 128 / G;
-  static_assert(block_smem_bytes(G, block_k_stages(G)) + sizeof(BlockSmemCtl) <= 227 * 1024,
-                "shared memory");
+  static_assert(block_smem_bytes(G) + sizeof(BlockSmemCtl) <= 227 * 1024, "shared memory");
   const int64_t T = (int64_t)a.batch * a.seq_len;
   CUtensorMap tq, tk, tv;
   const uint64_t dq[3] = {(uint64_t)kD, (uint64_t)a.num_q_heads, (uint64_t)T};
@@ -745,7 +744,7 @@ sa_status launch_typed(const BlockArgs& a) {
   p.out = reinterpret_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.err = device_error_word();
-  const size_t smem = block_smem_bytes(G, block_k_stages(G));
+  const size_t smem = block_smem_bytes(G);
   auto kern = block_sparse_fwd_kernel<G, MODE>;
   if (!set_dynamic_smem_once((const void*)kern, (int)smem))
     return fail(SA_ERR_CUDA, "sa_block_sparse_fwd: %s", cudaGetErrorString(cudaGetLastError()));
