@@ -168,3 +168,31 @@ def test_many_documents(docs_per_row, mode):
     ro, rl = oracle_run(c, mode)
     rel, dl = compare(out, lse, ro, rl)
     assert rel <= REL_L2_TOL and dl <= LSE_TOL, (docs_per_row, mode, rel, dl)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (16, 4), (16, 1)])
+@pytest.mark.parametrize("mode", [NULL, KEY0])
+def test_many_tiles_per_cta(hq, hkv, mode):
+    # 2 x 4096 tokens: every CTA walks several tiles (G = 1, 2, 4, 16: 3.4 to
+    # 6.7 tiles per CTA), so each tile's metadata, Q and O are handed over
+    # from the previous tile's
+    c = W.block_case(2, 4096, hq, hkv, 128, 64, 8, 3, (-2.2, 2.49), mode, seed=6000 + hq + hkv,
+                     pad_rows=40)
+    out, lse = gpu_run(c, mode)
+    ro, rl = oracle_run(c, mode)
+    rel, dl = compare(out, lse, ro, rl)
+    assert rel <= REL_L2_TOL and dl <= LSE_TOL, (hq, hkv, mode, rel, dl)
+
+
+def test_union_capacity_is_checked():
+    import torch
+    import attention_head_sinks_gb300 as sa
+    # one token per KV group row tile of 128 tokens x topk 16 = 2048 possible
+    # union blocks, and 1032 blocks per row: above the 1024-block capacity
+    S = 66048
+    q = torch.zeros((S, 1, 128), dtype=torch.bfloat16, device="cuda")
+    tab = torch.full((S, 16), -1, dtype=torch.int32, device="cuda")
+    cu = torch.tensor([0, S], dtype=torch.int32, device="cuda")
+    with pytest.raises(sa.SAError) as e:
+        sa.sa_block_sparse_fwd(q, q, q, 1, S, tab, 64, cu, None, NONE, 0.08)
+    assert "union blocks" in str(e.value)
