@@ -24,10 +24,15 @@
 //   S_j = Q K_j^T (N = 128) into one of two TMEM buffers,
 //   softmax over S_j with per-element selection / causal / document masks,
 //   P_j (bf16) written over S_j, O += P_j V_j with P_j read from TMEM.
-// Warp roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
-// warps 4..11 softmax and epilogue: warps w and w + 4 read TMEM lanes
-// 32 (w mod 4) ... and split each step's two blocks (and the O columns)
-// between them; each reads its 64 scores once per step.
+// Persistent: one CTA per SM walks tiles blockIdx.x + n * gridDim.x.
+// Warp roles: warp 2 allocates TMEM, then builds each tile's metadata (token
+// positions, union list, token masks) a tile ahead into one of two buffers;
+// thread 0 streams K, thread 96 streams Q and V (separate two-stage rings);
+// thread 32 issues the MMAs; warps 4..11 run the softmax and the epilogue:
+// warps w and w + 4 read TMEM lanes 32 (w mod 4) ... and split each step's
+// two blocks (and the O columns) between them; each reads its 64 scores once
+// per step.  mbarriers hand over every buffer (metadata, Q, K, V, S, P, O);
+// step parities run on per-CTA step counters.
 // The running max is rescaled lazily: O and l are rescaled only when a row's
 // max grows by more than 2^8, so P stays below 256.
 #include <cuda_bf16.h>
