@@ -9,7 +9,8 @@ Covers the full 64-query x 128-head decode workload over an fp8 cache with
 the -inf no-op, bitwise agreement with the bf16 path on power-of-two scales
 (the dequantised rows are then bf16 values and the scale commutes with every
 rounding), ragged and repeated lists, head counts off one 128-row block,
-and more than eight 256-key items per query.
+more than eight 256-key items per query, and caches that hold every non-NaN
+e4m3 code (subnormals, both zeros, +-448) under row scales over 16 octaves.
 """
 import numpy as np
 import pytest
@@ -136,3 +137,21 @@ def test_more_than_eight_items():
     c = W.index_fp8_case(4, 40, 576, 512, 9000, 3000, (2900, 300, 2100, 7), (-2.2, 2.49),
                          NULL, 3900, "many_items_fp8")
     check(c, NULL)
+
+
+@pytest.mark.parametrize("mode", [NULL, NONE])
+def test_every_e4m3_code(mode):
+    # latent rows cycle through all 254 non-NaN codes (subnormals, both
+    # zeros, +-448) in shifted orders, with row scales from 2^-12 to 2^4 times
+    # 1/448 (so values stay O(1)): every code reaches the MMAs and the scale
+    # folding through the kernel's own conversion
+    rng = np.random.default_rng(77)
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    nkv, dqk = 1024, 576
+    kv = np.stack([np.roll(np.resize(codes, dqk), 7 * r) for r in range(nkv)]).astype(np.uint8)
+    kv_scale = (2.0 ** rng.integers(-12, 5, size=nkv) / 448.0).astype(np.float32)
+    base = W.index_fp8_case(8, 128, 576, 512, nkv, 300, (1, 5, 40, 256, 300, 17, 3, 128),
+                            (-2.2, 2.49), mode, 4100)
+    c = W.IndexFp8Case("all_codes", base.q, kv, kv_scale, base.indices, 512, base.sinks, mode,
+                       base.scale)
+    check(c, mode)
