@@ -63,7 +63,9 @@ struct RingParams {
   int32_t nt;       // tiles per head
   int32_t items;    // nt * num_kv_heads
   int32_t num_kv_heads;
-  int32_t chunks;   // token chunks per head: grid = chunks * num_kv_heads
+  int32_t chunks;   // token chunks per head (main CTAs: chunks * num_kv_heads)
+  int32_t chunk_size;      // tiles per main CTA, or 0: nt split evenly over chunks
+  int32_t spill_per_head;  // last tiles of every head left to the spill CTAs
   int32_t nbt;      // key blocks per tile
   int32_t bf_off;   // first block of tile j = j * NEWB + bf_off
   const float* sinks;
@@ -114,6 +116,57 @@ __device__ __forceinline__ ItemInfo walk_item(ItemWalk& w, int u, const RingPara
   return it;
 }
 
+// The items of one CTA.  Main CTAs (the first chunks * num_kv_heads) take a
+// contiguous run of one head's tiles, heads fastest.  When the SM count is not
+// a multiple of the head count, the CTAs past them (spill CTAs) share the last
+// spill_per_head tiles of every head, listed head by head, so that no main CTA
+// needs a tile more than the average: a spill CTA's list is a few short head
+// runs, each restarting the ring.
+struct CtaItems {
+  int u0, n;
+  bool spill;
+};
+
+__device__ __forceinline__ CtaItems cta_items(const RingParams& p) {
+  const int b = blockIdx.x;
+  const int nmain = p.chunks * p.num_kv_heads;
+  CtaItems c;
+  if (b < nmain) {
+    // heads fastest: CTAs that run at the same time cover every head of the
+    // same token range, so the DRAM pages holding the rows of neighbouring
+    // heads are read while they are open (a version with contiguous item
+    // ranges over all SMs ran 10 % slower)
+    const int cg = b % p.num_kv_heads;
+    const int cr = b / p.num_kv_heads;
+    int j0, j1;
+    if (p.chunk_size > 0) {
+      j0 = cr * p.chunk_size;
+      j1 = j0 + p.chunk_size;
+    } else {
+      j0 = (int)(((int64_t)cr * p.nt) / p.chunks);
+      j1 = (int)(((int64_t)(cr + 1) * p.nt) / p.chunks);
+    }
+    c.u0 = cg * p.nt + j0;
+    c.n = j1 - j0;
+    c.spill = false;
+  } else {
+    const int e = b - nmain, ne = (int)gridDim.x - nmain;
+    const int64_t tot = (int64_t)p.num_kv_heads * p.spill_per_head;
+    c.u0 = (int)((int64_t)e * tot / ne);
+    c.n = (int)((int64_t)(e + 1) * tot / ne) - c.u0;
+    c.spill = true;
+  }
+  return c;
+}
+
+// Global item u = head * nt + tile of the CTA's it-th item.
+__device__ __forceinline__ int cta_item_u(const CtaItems& c, int it, const RingParams& p) {
+  if (!c.spill) return c.u0 + it;
+  const int l = c.u0 + it;
+  const int g = l / p.spill_per_head;
+  return g * p.nt + (p.nt - p.spill_per_head) + (l - g * p.spill_per_head);
+}
+
 template <int D, int G, int MODE>
 __global__ void __launch_bounds__(384, 1)
 window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -136,16 +189,8 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   griddep_launch_dependents();
-  // CTA -> (KV head, token chunk), heads fastest: CTAs that run at the same
-  // time cover every head of the same token range, so the DRAM pages holding
-  // the rows of neighbouring heads are read while they are open (a version
-  // with contiguous item ranges over all SMs ran 10 % slower).
-  const int cg = blockIdx.x % p.num_kv_heads;
-  const int cr = blockIdx.x / p.num_kv_heads;
-  const int j0 = (int)(((int64_t)cr * p.nt) / p.chunks);
-  const int j1 = (int)(((int64_t)(cr + 1) * p.nt) / p.chunks);
-  const int u0 = cg * p.nt + j0;
-  const int n = j1 - j0;
+  const CtaItems ci = cta_items(p);
+  const int n = ci.n;
 
   if (tid == 0) {
     for (int i = 0; i < kNQ; ++i) {
@@ -183,7 +228,7 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
     int seq = 0, last_bl = 0, nq = 0;
     bool ok = true;
     for (int it = 0; it < n && ok; ++it) {
-      const ItemInfo info = walk_item<S::NEWB>(w, u0 + it, p);
+      const ItemInfo info = walk_item<S::NEWB>(w, cta_item_u(ci, it, p), p);
       const int qs = it % kNQ;
       if (it >= kNQ) ok = mbar_wait(&ctl.q_empty[qs], ((it / kNQ) - 1) & 1, p.err, kErrWaitFree);
       if (!ok) break;
@@ -253,12 +298,12 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
       mma_commit(&ctl.s_full[b]);
       return true;
     };
-    ItemInfo cur = walk_item<S::NEWB>(w, u0, p);
+    ItemInfo cur = walk_item<S::NEWB>(w, cta_item_u(ci, 0, p), p);
     ok = issue_s(0, cur);
     for (int it = 0; it < n && ok; ++it) {
       const bool have_next = it + 1 < n;
       ItemInfo nxt = cur;
-      if (have_next) nxt = walk_item<S::NEWB>(w, u0 + it + 1, p);
+      if (have_next) nxt = walk_item<S::NEWB>(w, cta_item_u(ci, it + 1, p), p);
       const bool ahead = have_next && nxt.same_run;
       if (ahead && !(ok = issue_s(it + 1, nxt))) break;
       const int b = it & 1;
@@ -295,7 +340,7 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int nchunks = (nk + 31) >> 5;
     for (int it = wg; it < n; it += 2) {
       const int k = it >> 1;
-      const int u = u0 + it;
+      const int u = cta_item_u(ci, it, p);
       const int g = u / p.nt;
       const int j = u - g * p.nt;
       const int tok0 = j * S::TQ;
@@ -406,10 +451,23 @@ sa_status launch_ring_typed(const WindowArgs& a, int nbt, int bf_off) {
     return fail(SA_ERR_CUDA, "sa_varlen_window_fwd: %s", cudaGetErrorString(cudaGetLastError()));
   cudaError_t e;
   p.num_kv_heads = a.num_kv_heads;
-  p.chunks = num_sms() / a.num_kv_heads;
+  const int sms = num_sms();
+  p.chunks = sms / a.num_kv_heads;
   if (p.chunks < 1) p.chunks = 1;
   if (p.chunks > p.nt) p.chunks = p.nt;
-  const int grid = p.chunks * a.num_kv_heads;
+  p.chunk_size = 0;
+  p.spill_per_head = 0;
+  int grid = p.chunks * a.num_kv_heads;
+  // Tiles per CTA at best: ceil(items / SMs).  If the main CTAs at that size
+  // leave tiles over and SMs are free, those SMs take the leftover tiles
+  // (at most as many each, since chunks * num_kv_heads + spare = SMs).
+  const int64_t cmax = (p.items + (int64_t)sms - 1) / sms;
+  const int spare = sms - grid;
+  if (spare > 0 && (int64_t)p.chunks * cmax < p.nt) {
+    p.chunk_size = (int32_t)cmax;
+    p.spill_per_head = p.nt - p.chunks * (int32_t)cmax;
+    grid += (int)std::min<int64_t>(spare, (int64_t)p.spill_per_head * a.num_kv_heads);
+  }
   e = launch_dependent(kern, dim3(grid), dim3(384), S::SMEM, a.stream, tq, tk, tv, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess)

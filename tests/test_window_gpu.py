@@ -3,7 +3,8 @@
 Covers the tiny two-sequence case in every sink mode, ragged sizes that span
 several tiles with a ragged tail, every supported GQA ratio and head dim,
 asymmetric and zero windows, length-1 sequences (with a -inf KEY0 sink: an
-empty key set), the bitwise no-op cases, and the full-size vision-tower and
+empty key set), shapes whose persistent schedule hands leftover tiles to the
+spare SMs (lists of short runs over several heads), the bitwise no-op cases, and the full-size vision-tower and
 GQA workloads in the launch configuration the benchmark times.
 """
 import numpy as np
@@ -121,6 +122,26 @@ def test_repeatable_and_stream_aware():
     o2, l2 = gpu_run(c, KEY0)
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
     assert torch.equal(l1, l2)
+
+
+SPILL = [
+    # lengths, hq, hkv, d.  On a 152-SM part: 16 KV heads x 64 tiles leave one
+    # tile of every head to the 8 SMs past the 144 main CTAs (each takes two
+    # one-tile runs of different heads); 12 heads x 100 tiles leave four per
+    # head (six-tile lists crossing a head); GQA 24 / 12 with 64-token tiles,
+    # 200 per head, leaves eight per head.
+    ([3000, 5192], 16, 16, 80),
+    ([5000, 3, 4797, 3000], 12, 12, 64),
+    ([6000, 1, 6799], 24, 12, 128),
+]
+
+
+@pytest.mark.parametrize("mode", [KEY0, NULL])
+@pytest.mark.parametrize("ci", range(len(SPILL)))
+def test_spill_schedule_shapes(ci, mode):
+    lengths, hq, hkv, d = SPILL[ci]
+    c = W.window_case(lengths, hq, hkv, d, 64, (-1.0, 3.0), mode, 2300 + ci, "spill%d" % ci)
+    check(c, mode)
 
 
 @pytest.mark.parametrize("tokens", [4096, 16384])
