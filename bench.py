@@ -937,17 +937,24 @@ def main():
     sampler = ClockSampler(gpu_uuid())
     total_ms = timed(runner.mode, args.steps)
     clocks = sampler.stop()
-    ndev = min(args.steps, 500)
-    per = device_times(runner.mode, ndev)
-    per_none = device_times(W.SINK_NONE, max(ndev // 2, 10))
+    # isolated launches of the timed mode and of the same kernel with sinks
+    # disabled, in alternating chunks so that a drift in clocks or in the
+    # co-tenants' load falls on both alike
+    ndev = max(min(args.steps, 500), 10)
+    chunk = min(ndev, 50)
+    per, per_none = [], []
+    for _ in range((ndev + chunk - 1) // chunk):
+        per += device_times(runner.mode, chunk)
+        per_none += device_times(W.SINK_NONE, chunk)
 
     step_ms = max_over_ranks(total_ms / args.steps, dist, "cuda")
     # per call over the timed region (back-to-back calls, the roofline's
     # denominator: algorithmic bytes and flops are counted per call), and per
-    # isolated launch (events around each call, the sink-cost comparison)
+    # isolated launch (events around each call; medians, the sink-cost
+    # comparison)
     call_us = step_ms * 1000.0
-    kern_us = statistics.mean(per)
-    kern_us_none = statistics.mean(per_none)
+    kern_us = statistics.median(per)
+    kern_us_none = statistics.median(per_none)
 
     # end to end: pinned host inputs -> device, the call, results -> host
     host_in, dev_out, run = runner.host_io()
