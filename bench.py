@@ -937,9 +937,16 @@ def main():
     sampler = ClockSampler(gpu_uuid())
     total_ms = timed(runner.mode, args.steps)
     clocks = sampler.stop()
-    # isolated launches of the timed mode and of the same kernel with sinks
-    # disabled, in alternating chunks so that a drift in clocks or in the
-    # co-tenants' load falls on both alike
+    # the sink cost: timed regions of back-to-back calls in the timed mode and
+    # with sinks disabled, in alternating rounds so that a drift in clocks or
+    # in the machine's other load falls on both alike
+    rounds = 4
+    per_round = max(args.steps // rounds, 10)
+    t_mode = t_none = 0.0
+    for _ in range(rounds):
+        t_mode += timed(runner.mode, per_round)
+        t_none += timed(W.SINK_NONE, per_round)
+    # isolated launches of both modes, alternating in the same way
     ndev = max(min(args.steps, 500), 10)
     chunk = min(ndev, 50)
     per, per_none = [], []
@@ -1028,7 +1035,8 @@ def main():
         "config": cfg,
         "roofline": roof,
         "secondary": other,
-        "sink_cost": round(kern_us / kern_us_none - 1.0, 4),
+        "sink_cost": round(t_mode / t_none - 1.0, 4),
+        "sink_cost_isolated": round(kern_us / kern_us_none - 1.0, 4),
         "launch_us_isolated_sinks_disabled": round(kern_us_none, 3),
         "e2e": {"value": round(e2e_us, 2), "unit": "us/call",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
