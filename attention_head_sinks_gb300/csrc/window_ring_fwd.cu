@@ -310,6 +310,11 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
       ok = mbar_wait(&ctl.p_full[b], (it >> 1) & 1, p.err, kErrWaitMma);
       if (!ok) break;
       tc_fence_after();
+      // P V block by block, oldest first; a block the next item does not use
+      // is released as soon as its own MMAs complete, so its slot's refill
+      // starts while the rest of P V runs.  O is signalled last, so that
+      // every earlier arrival has landed once O is seen complete.
+      const int nrel = ahead ? S::NEWB : p.nbt;
       for (int kb = 0; kb < p.nbt; ++kb) {
         const int sq = cur.seq_bf + kb;
         const uint8_t* vbase = sV + (sq % NR) * S::KB * 32;
@@ -321,11 +326,8 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
                  tmem + (uint32_t)(b * kBufCols + (kb * S::KB + ks * 16) / 2), bd, idesc_o,
                  (kb | ks) ? 1u : 0u);
         }
+        if (kb < nrel) mma_commit(&ctl.kv_empty[sq % NR]);
       }
-      // Release the blocks the next item does not use, then signal O (last,
-      // so that every earlier arrival has landed once O is seen complete).
-      const int nrel = ahead ? S::NEWB : p.nbt;
-      for (int r = 0; r < nrel; ++r) mma_commit(&ctl.kv_empty[(cur.seq_bf + r) % NR]);
       mma_commit(&ctl.o_full[b]);
       if (have_next && !ahead && !(ok = issue_s(it + 1, nxt))) break;
       cur = nxt;
