@@ -144,6 +144,28 @@ def test_spill_schedule_shapes(ci, mode):
     check(c, mode)
 
 
+def rising_logit_case(mode, seed):
+    """q = 24 e0 on every row and head; key j has 24 * ((j // 32) % 4) in
+    dimension 0 (random elsewhere), so the scaled logits (log2 units) step by
+    about 93 from one 32-key chunk to the next: a row's chunks span up to
+    280 log2 units, nearly all of its weight sits on a few keys of its
+    highest chunk, and the rest underflows."""
+    c = W.window_case([700, 300, 45], 4, 4, 80, 64, (-1.0, 3.0), mode, seed, "rising")
+    T = c.q.shape[0]
+    q = np.zeros((T, 4, 80), np.float32)
+    q[:, :, 0] = 24.0
+    k = (c.k.astype(np.uint32) << 16).view(np.float32).copy()
+    k[:, :, 0] = 24.0 * ((np.arange(T) // 32) % 4)[:, None]
+    c.q = W.f32_to_bf16_bits(q)
+    c.k = W.f32_to_bf16_bits(k)
+    return c
+
+
+@pytest.mark.parametrize("mode", [NONE, KEY0, NULL])
+def test_rising_logits_across_chunks(mode):
+    check(rising_logit_case(mode, 2500), mode)
+
+
 @pytest.mark.parametrize("tokens", [4096, 16384])
 @pytest.mark.parametrize("mode", [KEY0, NONE])
 def test_vision_tower_window_block(tokens, mode):
