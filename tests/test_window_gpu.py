@@ -161,6 +161,26 @@ def rising_logit_case(mode, seed):
     return c
 
 
+def test_key0_dominant_first_key_with_negative_sinks():
+    """Every sequence's first key carries the largest raw logit of its rows
+    (q = 4 e0, that key 8 e0, the others random), under KEY0_BIAS sinks
+    -0.5, -5, -30 and +4 on the four heads: the biased key falls below the
+    other keys or far below them, or dominates the row."""
+    c = W.window_case([300, 1, 77, 129, 1000, 5, 64, 65], 4, 4, 80, 64, (-1.0, 3.0), KEY0,
+                      2600, "k0_dominant")
+    T = c.q.shape[0]
+    q = (c.q.astype(np.uint32) << 16).view(np.float32).copy()
+    q[:] = 0.0
+    q[:, :, 0] = 4.0
+    k = (c.k.astype(np.uint32) << 16).view(np.float32).copy()
+    k[c.cu_seqlens[:-1], :, :] = 0.0
+    k[c.cu_seqlens[:-1], :, 0] = 8.0
+    c.q = W.f32_to_bf16_bits(q)
+    c.k = W.f32_to_bf16_bits(k)
+    sinks = np.array([-0.5, -5.0, -30.0, 4.0], np.float32)
+    check(c, KEY0, sinks=sinks)
+
+
 @pytest.mark.parametrize("mode", [NONE, KEY0, NULL])
 def test_rising_logits_across_chunks(mode):
     check(rising_logit_case(mode, 2500), mode)
