@@ -135,6 +135,16 @@ def test_many_queries(nq):
     check(c, NULL)
 
 
+@pytest.mark.parametrize("hq", [128, 192])
+def test_all_lists_full_many_units_per_cta(hq):
+    # every query lists 2048 valid keys: 8 full items per query and 128-head
+    # block, 512 or 1024 work units for one CTA per SM, so each CTA runs
+    # several units back to back on re-initialised barriers
+    c = W.index_case(64, hq, 576, 512, 65536, 2048, (2048,), (-2.2, 2.49), NULL, 3600 + hq,
+                     "all_full")
+    check(c, NULL)
+
+
 @pytest.mark.parametrize("hq", [128, 40])
 def test_more_than_eight_items(hq):
     # topk 3000: 2900 and 2100 valid keys give 12 and 9 items of 256 keys
