@@ -133,8 +133,8 @@ def test_list_lengths(topk):
     check(c, NULL)
 
 
-def test_all_lists_full_many_units_per_cta():
-    # 64 queries x 2048 valid keys: 512 full items, several per CTA
+def test_all_lists_full():
+    # 64 queries x 2048 valid keys: 512 full items, several waves of CTAs
     c = W.index_fp8_case(64, 128, 576, 512, 65536, 2048, (2048,), (-2.2, 2.49), NULL, 3950,
                          "all_full_fp8")
     check(c, NULL)

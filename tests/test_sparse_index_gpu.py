@@ -136,10 +136,10 @@ def test_many_queries(nq):
 
 
 @pytest.mark.parametrize("hq", [128, 192])
-def test_all_lists_full_many_units_per_cta(hq):
+def test_all_lists_full(hq):
     # every query lists 2048 valid keys: 8 full items per query and 128-head
-    # block, 512 or 1024 work units for one CTA per SM, so each CTA runs
-    # several units back to back on re-initialised barriers
+    # block, 512 or 1024 CTAs with work, several waves of them, and every
+    # query goes through the combine
     c = W.index_case(64, hq, 576, 512, 65536, 2048, (2048,), (-2.2, 2.49), NULL, 3600 + hq,
                      "all_full")
     check(c, NULL)
