@@ -96,22 +96,14 @@ __device__ __forceinline__ RowMeta row_meta(const int32_t* cu, int num_seqs,
 // chunk c of P (bf16 pairs) is written at p_addr + 16 c, in place over S
 // chunks that have already been read.  Tensor-memory loads are
 // double-buffered: chunk c + 1 is requested before chunk c is processed.
+// The softmax itself has no sink term: a KEY0_BIAS sink is already in S
+// (key0_bias_in_tmem), a NULL_LOGIT one enters in finalize_row.
 
-template <int MODE>
 __device__ __forceinline__ void max_one(const float (&s)[32], int c, const RowMeta& r,
-                                        float c2, uint32_t span, float (&mr)[4], float& ms) {
+                                        uint32_t span, float (&mr)[4]) {
   const int c0 = 32 * c;
   const bool full = __all_sync(0xffffffffu, c0 >= r.clo && c0 + 31 <= r.chi);
-  const bool has_k0 = (MODE == SA_SINK_KEY0_BIAS) &&
-                      __any_sync(0xffffffffu, r.ck0 >= c0 && r.ck0 < c0 + 32);
-  if (has_k0) {
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      float x = s[e] * c2;
-      if (c0 + e == r.ck0) x = x + r.sink2;
-      ms = fmaxf(ms, ((uint32_t)(c0 + e - r.clo) <= span) ? x : -INFINITY);
-    }
-  } else if (full) {
+  if (full) {
 #pragma unroll
     for (int e = 0; e < 32; e += 2) mr[(e >> 1) & 3] = max3f(mr[(e >> 1) & 3], s[e], s[e + 1]);
   } else {
@@ -125,17 +117,13 @@ __device__ __forceinline__ void max_one(const float (&s)[32], int c, const RowMe
 
 // P = 2^(x - m_use) as bf16 for one chunk (in registers s, stored to
 // p_addr + 16 c); adds the chunk's values to the partial pair sums lp.  The
-// exponent is fma(s, c2, -m) in every branch (pairs by the packed fma, each
-// lane rounded as the scalar one) and every branch accumulates in the same
-// order, so a zero KEY0_BIAS sink reproduces the no-sink bits exactly.
-template <int MODE>
+// exponent is fma(s, c2, -m) in both branches (pairs by the packed fma, each
+// lane rounded as the scalar one) and both accumulate in the same order.
 __device__ __forceinline__ void exp_one(float (&s)[32], int c, const RowMeta& r, float c2,
                                         float m_use, uint32_t span, uint64_t (&lp)[4],
                                         uint32_t p_addr) {
   const int c0 = 32 * c;
   const bool full = __all_sync(0xffffffffu, c0 >= r.clo && c0 + 31 <= r.chi);
-  const bool has_k0 = (MODE == SA_SINK_KEY0_BIAS) &&
-                      __any_sync(0xffffffffu, r.ck0 >= c0 && r.ck0 < c0 + 32);
   const uint64_t c2c2 = f2_pack(c2, c2), nmnm = f2_pack(-m_use, -m_use);
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {
@@ -143,16 +131,13 @@ __device__ __forceinline__ void exp_one(float (&s)[32], int c, const RowMeta& r,
     s[e] = f2_lo(t);
     s[e + 1] = f2_hi(t);
   }
-  if (full && !has_k0) {
+  if (full) {
 #pragma unroll
     for (int e = 0; e < 32; ++e) s[e] = ex2_approx(s[e]);
   } else {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      float x = s[e];
-      if (MODE == SA_SINK_KEY0_BIAS && c0 + e == r.ck0) x = x + r.sink2;
-      s[e] = ((uint32_t)(c0 + e - r.clo) <= span) ? ex2_approx(x) : 0.f;
-    }
+    for (int e = 0; e < 32; ++e)
+      s[e] = ((uint32_t)(c0 + e - r.clo) <= span) ? ex2_approx(s[e]) : 0.f;
   }
   uint32_t pk[16];
 #pragma unroll
@@ -163,19 +148,17 @@ __device__ __forceinline__ void exp_one(float (&s)[32], int c, const RowMeta& r,
   tmem_st16(p_addr + 16 * c, pk);
 }
 
-// Max of the scaled (log2) logits of chunks [c_lo, c_hi].  Chunks without
-// the biased key take the max of the raw logits (scaling by c2 > 0 is
-// monotone, so max(s) * c2 == max(s * c2) exactly); the chunk holding the
-// biased key is scaled element by element.  Four partial maxima of
-// three-input max operations keep the dependency chains short.  Returns
-// -inf when no element is live.
-template <int MODE, bool DB = true>
+// Max of the scaled (log2) logits of chunks [c_lo, c_hi]: the max of the raw
+// logits times c2 (scaling by c2 > 0 is monotone, so max(s) * c2 ==
+// max(s * c2) exactly).  Four partial maxima of three-input max operations
+// keep the dependency chains short.  Returns -inf when no element is live.
+template <bool DB = true>
 __device__ __forceinline__ float max_chunks(uint32_t s_addr, int c_lo, int c_hi,
                                             const RowMeta& r, float c2) {
   float sa[32];
   [[maybe_unused]] float sb[DB ? 32 : 1];
   const uint32_t span = (uint32_t)(r.chi - r.clo);
-  float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, ms = -INFINITY;
+  float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   if constexpr (DB) {
     if (c_lo <= c_hi) {
       tmem_ld32(s_addr + 32 * c_lo, sa);
@@ -183,29 +166,29 @@ __device__ __forceinline__ float max_chunks(uint32_t s_addr, int c_lo, int c_hi,
     }
     for (int c = c_lo; c <= c_hi; c += 2) {
       if (c + 1 <= c_hi) tmem_ld32(s_addr + 32 * (c + 1), sb);
-      max_one<MODE>(sa, c, r, c2, span, mr, ms);
+      max_one(sa, c, r, span, mr);
       if (c + 1 > c_hi) break;
       tmem_wait_ld();
       if (c + 2 <= c_hi) tmem_ld32(s_addr + 32 * (c + 2), sa);
-      max_one<MODE>(sb, c + 1, r, c2, span, mr, ms);
+      max_one(sb, c + 1, r, span, mr);
       tmem_wait_ld();
     }
   } else {
     for (int c = c_lo; c <= c_hi; ++c) {
       tmem_ld32(s_addr + 32 * c, sa);
       tmem_wait_ld();
-      max_one<MODE>(sa, c, r, c2, span, mr, ms);
+      max_one(sa, c, r, span, mr);
     }
   }
   const float mraw = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
-  return fmaxf(mraw * c2, ms);
+  return mraw * c2;
 }
 
 // P = 2^(x - m_use) as bf16 for chunks [c_lo, c_hi]; returns their row sum
 // (eight partial sums, kept as four packed pairs).  Every branch forms the exponent as fma(s, c2, -m)
 // (+ sink on key 0) so that a zero KEY0_BIAS sink reproduces the no-sink
 // bits exactly.
-template <int MODE, bool DB = true>
+template <bool DB = true>
 __device__ __forceinline__ float exp_chunks(uint32_t s_addr, uint32_t p_addr, int c_lo,
                                             int c_hi, const RowMeta& r, float c2,
                                             float m_use) {
@@ -220,18 +203,18 @@ __device__ __forceinline__ float exp_chunks(uint32_t s_addr, uint32_t p_addr, in
     }
     for (int c = c_lo; c <= c_hi; c += 2) {
       if (c + 1 <= c_hi) tmem_ld32(s_addr + 32 * (c + 1), sb);
-      exp_one<MODE>(sa, c, r, c2, m_use, span, lp, p_addr);
+      exp_one(sa, c, r, c2, m_use, span, lp, p_addr);
       if (c + 1 > c_hi) break;
       tmem_wait_ld();
       if (c + 2 <= c_hi) tmem_ld32(s_addr + 32 * (c + 2), sa);
-      exp_one<MODE>(sb, c + 1, r, c2, m_use, span, lp, p_addr);
+      exp_one(sb, c + 1, r, c2, m_use, span, lp, p_addr);
       tmem_wait_ld();
     }
   } else {
     for (int c = c_lo; c <= c_hi; ++c) {
       tmem_ld32(s_addr + 32 * c, sa);
       tmem_wait_ld();
-      exp_one<MODE>(sa, c, r, c2, m_use, span, lp, p_addr);
+      exp_one(sa, c, r, c2, m_use, span, lp, p_addr);
     }
   }
   const uint64_t s = f2_add(f2_add(lp[0], lp[1]), f2_add(lp[2], lp[3]));
@@ -249,18 +232,43 @@ __device__ __forceinline__ void zero_chunks(uint32_t p_addr, int c_lo, int c_hi)
 // Whole-row softmax over chunks [0, nchunks), the live ones being
 // [ch_lo, ch_hi].  Returns the row max m (log2 units, -inf for an empty row)
 // and the row sum l of 2^(x - m).
-template <int MODE, bool DB = true, bool DB_MAX = DB>
+template <bool DB = true, bool DB_MAX = DB>
 __device__ __forceinline__ void softmax_rows(uint32_t s_addr, uint32_t p_addr, int nchunks,
                                              int ch_lo, int ch_hi, const RowMeta& r,
                                              float c2, float& m_out, float& l_out) {
-  const float m = max_chunks<MODE, DB_MAX>(s_addr, ch_lo, ch_hi, r, c2);
+  const float m = max_chunks<DB_MAX>(s_addr, ch_lo, ch_hi, r, c2);
   // Rows with no finite logit use 0 as the reference so that -inf - m stays -inf.
   const float m_use = (m == -INFINITY) ? 0.f : m;
-  l_out = exp_chunks<MODE, DB>(s_addr, p_addr, ch_lo, ch_hi, r, c2, m_use);
+  l_out = exp_chunks<DB>(s_addr, p_addr, ch_lo, ch_hi, r, c2, m_use);
   zero_chunks(p_addr, 0, ch_lo - 1);
   zero_chunks(p_addr, ch_hi + 1, nchunks - 1);
   tmem_wait_st();
   m_out = m;
+}
+
+// KEY0_BIAS: the sink goes onto each row's first-key logit in S itself, in
+// raw logit units (s + sink / (scale log2 e)), before the softmax, which is
+// then the no-sink one.  Only warps whose rows see a first key do anything:
+// one tensor-memory load and store of each distinct first-key column among
+// the warp's rows (one per sequence start in reach), lanes without that
+// column storing back what they read.
+__device__ __forceinline__ void key0_bias_in_tmem(uint32_t s_addr, const RowMeta& r, float c2) {
+  int todo = r.ck0;
+  const float add = r.sink2 / c2;
+  for (;;) {
+    const unsigned col =
+        __reduce_min_sync(0xffffffffu, todo >= 0 ? (unsigned)todo : 0xffffffffu);
+    if (col == 0xffffffffu) break;
+    float v;
+    tmem_ld1(s_addr + col, v);
+    tmem_wait_ld();
+    if (todo == (int)col) {
+      v = v + add;
+      todo = -1;
+    }
+    tmem_st1(s_addr + col, v);
+    tmem_wait_st();
+  }
 }
 
 // 1/den (with the NULL_LOGIT fold) and the natural-log LSE over real keys.

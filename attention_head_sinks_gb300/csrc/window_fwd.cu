@@ -145,8 +145,10 @@ window_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   // ---- softmax: P = 2^(x - m) as bf16 into TMEM, row max and sum ----------
   float m, l;
-  win::softmax_rows<MODE>(lane_base + kColS, lane_base + kColP, nk / 32, wc_lo >> 5,
-                          wc_hi >> 5, r, p.scale_log2, m, l);
+  if constexpr (MODE == SA_SINK_KEY0_BIAS)
+    win::key0_bias_in_tmem(lane_base + kColS, r, p.scale_log2);
+  win::softmax_rows(lane_base + kColS, lane_base + kColP, nk / 32, wc_lo >> 5, wc_hi >> 5, r,
+                    p.scale_log2, m, l);
   tc_fence_before();
   __syncthreads();
 

@@ -357,8 +357,9 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       float m, l;
-      win::softmax_rows<MODE, false>(lane_base, lane_base, nchunks, wc_lo >> 5, wc_hi >> 5, r,
-                              p.scale_log2, m, l);
+      if constexpr (MODE == SA_SINK_KEY0_BIAS) win::key0_bias_in_tmem(lane_base, r, p.scale_log2);
+      win::softmax_rows<false>(lane_base, lane_base, nchunks, wc_lo >> 5, wc_hi >> 5, r,
+                               p.scale_log2, m, l);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.p_full[wg]);
