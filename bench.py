@@ -136,12 +136,12 @@ class WindowRunner:
                                 self.sinks, self.mode if mode is None else mode,
                                 c.scale, out=out, lse=lse)
 
-    def host_io(self):
+    def host_io(self, slot=0):
         import torch
         c = self.c
         host_in = [_torch_bits(x) for x in (c.q, c.k, c.v)] + \
             [torch.from_numpy(c.cu_seqlens), torch.from_numpy(c.sinks)]
-        out, lse = self.sets[0][3], self.sets[0][4]
+        out, lse = self.sets[slot][3], self.sets[slot][4]
 
         def run(dev_in):
             import attention_head_sinks_gb300 as sa
@@ -231,18 +231,19 @@ class IndexRunner:
                                self.mode if mode is None else mode, c.scale,
                                out=out, lse=lse, workspace=self.ws)
 
-    def host_io(self):
+    def host_io(self, slot=0):
         import torch
         c = self.c
         host_in = [_torch_bits(c.q), _torch_bits(c.kv), torch.from_numpy(c.indices),
                    torch.from_numpy(c.sinks)]
-        out, lse = self.sets[0][3], self.sets[0][4]
+        out, lse = self.sets[slot][3], self.sets[slot][4]
+        # a second slot runs concurrently: its own split-KV workspace
+        ws = self.ws if slot == 0 else torch.empty_like(self.ws)
 
         def run(dev_in):
             import attention_head_sinks_gb300 as sa
             sa.sa_sparse_index_fwd(dev_in[0], dev_in[1], dev_in[2], c.dv, dev_in[3],
-                                   self.mode, c.scale, out=out, lse=lse,
-                                   workspace=self.ws)
+                                   self.mode, c.scale, out=out, lse=lse, workspace=ws)
         return host_in, [out, lse], run
 
     def oracle_rows(self):
@@ -321,18 +322,20 @@ class IndexFp8Runner(IndexRunner):
                                    self.mode if mode is None else mode, c.scale,
                                    out=out, lse=lse, workspace=self.ws)
 
-    def host_io(self):
+    def host_io(self, slot=0):
         import torch
         c = self.c
         host_in = [_torch_bits(c.q), torch.from_numpy(c.kv), torch.from_numpy(c.kv_scale),
                    torch.from_numpy(c.indices), torch.from_numpy(c.sinks)]
-        out, lse = self.sets[0][4], self.sets[0][5]
+        out, lse = self.sets[slot][4], self.sets[slot][5]
+        # a second slot runs concurrently: its own split-KV workspace
+        ws = self.ws if slot == 0 else torch.empty_like(self.ws)
 
         def run(dev_in):
             import attention_head_sinks_gb300 as sa
             sa.sa_sparse_index_fwd_fp8(dev_in[0], dev_in[1], dev_in[2], dev_in[3], c.dv,
                                        dev_in[4], self.mode, c.scale, out=out, lse=lse,
-                                       workspace=self.ws)
+                                       workspace=ws)
         return host_in, [out, lse], run
 
     def oracle(self, rows):
@@ -408,13 +411,13 @@ class BlockRunner:
                                self.cu, self.sinks, self.mode if mode is None else mode,
                                c.scale, out=out, lse=lse)
 
-    def host_io(self):
+    def host_io(self, slot=0):
         import torch
         c = self.c
         host_in = [_torch_bits(x) for x in (c.q, c.k, c.v)] + \
             [torch.from_numpy(c.block_table), torch.from_numpy(c.cu_docs),
              torch.from_numpy(c.sinks)]
-        out, lse = self.sets[0][3], self.sets[0][4]
+        out, lse = self.sets[slot][3], self.sets[slot][4]
 
         def run(dev_in):
             import attention_head_sinks_gb300 as sa
@@ -488,12 +491,12 @@ class MergeRunner:
         sa.sa_merge_attn_states(oa, la, ob, lb, self.sinks,
                                 self.mode if mode is None else mode, out=out, lse=lse)
 
-    def host_io(self):
+    def host_io(self, slot=0):
         import torch
         c = self.c
         host_in = [_torch_bits(c.out_a), torch.from_numpy(c.lse_a), _torch_bits(c.out_b),
                    torch.from_numpy(c.lse_b), torch.from_numpy(c.sinks)]
-        out, lse = self.sets[0][4], self.sets[0][5]
+        out, lse = self.sets[slot][4], self.sets[slot][5]
 
         def run(dev_in):
             import attention_head_sinks_gb300 as sa
@@ -567,10 +570,10 @@ class SelectRunner:
         c = self.c
         sa.sa_block_select(qi, ki, c.batch, c.seq_len, c.block_size, c.topk, block_table=tab)
 
-    def host_io(self):
+    def host_io(self, slot=0):
         c = self.c
         host_in = [_torch_bits(c.index_q), _torch_bits(c.index_k)]
-        tab = self.sets[0][2]
+        tab = self.sets[slot][2]
 
         def run(dev_in):
             import attention_head_sinks_gb300 as sa
@@ -648,20 +651,21 @@ class SelectedBlockRunner(BlockRunner):
                                            self.mode if mode is None else mode, c.scale,
                                            out=out, lse=lse)
 
-    def host_io(self):
+    def host_io(self, slot=0):
         import torch
         c, sc = self.c, self.sc
         host_in = [_torch_bits(x) for x in (c.q, c.k, c.v)] + \
             [_torch_bits(sc.index_q), _torch_bits(sc.index_k), torch.from_numpy(c.cu_docs),
              torch.from_numpy(c.sinks)]
-        out, lse = self.sets[0][3], self.sets[0][4]
+        out, lse = self.sets[slot][3], self.sets[slot][4]
+        tabs = self.tabs if slot == 0 else torch.empty_like(self.tabs)
 
         def run(dev_in):
             import attention_head_sinks_gb300 as sa
             sa.sa_block_select(dev_in[3], dev_in[4], sc.batch, sc.seq_len, sc.block_size,
-                               sc.topk, block_table=self.tabs)
+                               sc.topk, block_table=tabs)
             sa.sa_block_sparse_fwd_index_heads(dev_in[0], dev_in[1], dev_in[2], c.batch,
-                                               c.seq_len, self.tabs, c.block_size, dev_in[5],
+                                               c.seq_len, tabs, c.block_size, dev_in[5],
                                                dev_in[6], self.mode, c.scale, out=out,
                                                lse=lse)
         return host_in, [out, lse], run
@@ -963,31 +967,42 @@ def main():
     kern_us = statistics.median(per)
     kern_us_none = statistics.median(per_none)
 
-    # end to end: pinned host inputs -> device, the call, results -> host
-    host_in, dev_out, run = runner.host_io()
-    host_in = [h.pin_memory() for h in host_in]
-    dev_in = [torch.empty_like(h, device="cuda") for h in host_in]
-    host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in dev_out]
+    # end to end: pinned host inputs -> device, the call, results -> host, each
+    # step on one of two streams in turn (its own device buffers), so that one
+    # step's copies overlap the other's call and copies in the other direction
+    nslot = 2
+    ios = [runner.host_io(k) for k in range(nslot)]
+    host_in = [h.pin_memory() for h in ios[0][0]]
+    dev_in = [[torch.empty_like(h, device="cuda") for h in host_in] for _ in range(nslot)]
+    host_out = [[torch.empty_like(o, device="cpu").pin_memory() for o in io[1]] for io in ios]
+    streams = [torch.cuda.Stream() for _ in range(nslot)]
 
-    def e2e_step():
-        for d_, h_ in zip(dev_in, host_in):
-            d_.copy_(h_, non_blocking=True)
-        run(dev_in)
-        for h_, o_ in zip(host_out, dev_out):
-            h_.copy_(o_, non_blocking=True)
+    def e2e_step(i):
+        k = i % nslot
+        with torch.cuda.stream(streams[k]):
+            for d_, h_ in zip(dev_in[k], host_in):
+                d_.copy_(h_, non_blocking=True)
+            ios[k][2](dev_in[k])
+            for h_, o_ in zip(host_out[k], ios[k][1]):
+                h_.copy_(o_, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(2 * nslot):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record()
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    for s_ in streams:
+        s_.wait_event(e0)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    for s_ in streams:
+        cur.wait_stream(s_)
+    e1.record(cur)
     torch.cuda.synchronize()
     e2e_us = e0.elapsed_time(e1) * 1000.0 / args.e2e_steps
     h2d = sum(h.numel() * h.element_size() for h in host_in)
-    d2h = sum(h.numel() * h.element_size() for h in host_out)
+    d2h = sum(h.numel() * h.element_size() for h in host_out[0])
 
     import attention_head_sinks_gb300 as sa
     err = sa.sa_device_error()
