@@ -534,41 +534,33 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (k0 >= bs && k0 < bs + kBlk) k0c = k0 - bs;  // then k0c == clo: live
           }
         }
-        const bool has_k0 = MODE == SA_SINK_KEY0_BIAS && __any_sync(0xffffffffu, k0c >= 0);
         const uint32_t span = (uint32_t)(chi - clo);
         const bool warp_live = __any_sync(0xffffffffu, clo != (1 << 30));
         const uint32_t sbase = lane_base + (uint32_t)(st * 128 + 64 * part);
         float s[2][32];
         float mx = -INFINITY;
-        float sk0 = -INFINITY;  // raw logit of the KEY0_BIAS key (taken out of s)
         if (warp_live) {
+          // KEY0_BIAS: the sink goes onto the first key's logit in S itself
+          // (raw units), so the softmax below is the no-sink one; only warps
+          // with a document's first key in this block do anything
+          if (MODE == SA_SINK_KEY0_BIAS && __any_sync(0xffffffffu, k0c >= 0))
+            tmem_add_lane_column(sbase, k0c, k0_sink2 / c2);
           tmem_ld32(sbase, s[0]);
           tmem_ld32(sbase + 32, s[1]);
           tmem_wait_ld();
           float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          if (has_k0) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                sk0 = (32 * c + e == k0c) ? s[c][e] : sk0;
-                s[c][e] = ((uint32_t)(32 * c + e - clo) <= span && 32 * c + e != k0c) ? s[c][e]
-                                                                                      : -INFINITY;
-              }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                s[c][e] = ((uint32_t)(32 * c + e - clo) <= span) ? s[c][e] : -INFINITY;
-          }
+            for (int e = 0; e < 32; ++e)
+              s[c][e] = ((uint32_t)(32 * c + e - clo) <= span) ? s[c][e] : -INFINITY;
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int e = 0; e < 32; e += 2)
               mr[(e >> 1) & 3] = max3f(mr[(e >> 1) & 3], s[c][e], s[c][e + 1]);
-          // max(s) * c2 == max(s * c2) exactly; the biased key enters scaled
-          mx = fmaxf(fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * c2, sk0 * c2 + k0_sink2);
+          // max(s) * c2 == max(s * c2) exactly
+          mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * c2;
         }
         ctl.red_m[st][part][row] = mx;
         bar_softmax();
@@ -602,9 +594,6 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
           // region, behind this thread's own reads; masked columns give 0
           const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;
           const uint64_t c2c2 = f2_pack(c2, c2), nmnm = f2_pack(-m_ref, -m_ref);
-          // the biased key's exponent: fma(s, c2, -m) + sink (bitwise the no-sink
-          // value for a zero sink)
-          const float xk0 = fmaf(sk0, c2, -m_ref) + k0_sink2;
           uint64_t lp[4] = {0, 0, 0, 0};
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -612,12 +601,7 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               const uint64_t x = f2_fma(f2_pack(s[c][e], s[c][e + 1]), c2c2, nmnm);
-              float x0 = f2_lo(x), x1 = f2_hi(x);
-              if (has_k0) {
-                x0 = (32 * c + e == k0c) ? xk0 : x0;
-                x1 = (32 * c + e + 1 == k0c) ? xk0 : x1;
-              }
-              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              const float p0 = ex2_approx(f2_lo(x)), p1 = ex2_approx(f2_hi(x));
               lp[(e >> 1) & 3] = f2_add(lp[(e >> 1) & 3], f2_pack(p0, p1));
               pk[e >> 1] = pack_bf16x2(p0, p1);
             }

@@ -253,6 +253,27 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
                : "memory");
 }
 
+// Add `add` to column `col` of this lane's row at taddr (col < 0: none), for
+// every lane of the warp at once: one 1-column load and store per distinct
+// column among the lanes, lanes without that column storing back what they
+// read.
+__device__ __forceinline__ void tmem_add_lane_column(uint32_t taddr, int col, float add) {
+  int todo = col;
+  for (;;) {
+    const unsigned c = __reduce_min_sync(0xffffffffu, todo >= 0 ? (unsigned)todo : 0xffffffffu);
+    if (c == 0xffffffffu) break;
+    float v;
+    tmem_ld1(taddr + c, v);
+    tmem_wait_ld();
+    if (todo == (int)c) {
+      v = v + add;
+      todo = -1;
+    }
+    tmem_st1(taddr + c, v);
+    tmem_wait_st();
+  }
+}
+
 // 32 lanes x 16 columns store.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr,
                                           const uint32_t (&r)[16]) {

@@ -253,22 +253,7 @@ __device__ __forceinline__ void softmax_rows(uint32_t s_addr, uint32_t p_addr, i
 // the warp's rows (one per sequence start in reach), lanes without that
 // column storing back what they read.
 __device__ __forceinline__ void key0_bias_in_tmem(uint32_t s_addr, const RowMeta& r, float c2) {
-  int todo = r.ck0;
-  const float add = r.sink2 / c2;
-  for (;;) {
-    const unsigned col =
-        __reduce_min_sync(0xffffffffu, todo >= 0 ? (unsigned)todo : 0xffffffffu);
-    if (col == 0xffffffffu) break;
-    float v;
-    tmem_ld1(s_addr + col, v);
-    tmem_wait_ld();
-    if (todo == (int)col) {
-      v = v + add;
-      todo = -1;
-    }
-    tmem_st1(s_addr + col, v);
-    tmem_wait_st();
-  }
+  tmem_add_lane_column(s_addr, r.ck0, r.sink2 / c2);
 }
 
 // 1/den (with the NULL_LOGIT fold) and the natural-log LSE over real keys.

@@ -359,7 +359,10 @@ class BlockRunner:
 
     def __init__(self, name):
         self.name = name
-        self.c = W.dsa_block_prefill(W.SINK_NULL_LOGIT)
+        # dsa_block_prefill_key0: the same batch with KEY0_BIAS sinks on the
+        # first key of each document
+        mode = W.SINK_KEY0_BIAS if name.endswith("_key0") else W.SINK_NULL_LOGIT
+        self.c = W.dsa_block_prefill(mode)
         self.mode = self.c.mode
 
     def counts(self):
@@ -687,6 +690,7 @@ RUNNERS = {
     "mla_sparse_decode": IndexRunner,
     "mla_sparse_decode_fp8": IndexFp8Runner,
     "dsa_block_prefill": BlockRunner,
+    "dsa_block_prefill_key0": BlockRunner,
     "merge_window_16384tok": MergeRunner,
     "dsa_block_select": SelectRunner,
     "dsa_block_prefill_selected": SelectedBlockRunner,
