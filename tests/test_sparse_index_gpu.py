@@ -126,6 +126,33 @@ def test_workspace_reuse_with_stale_contents():
     check(c, NULL, indices=idx2, workspace=ws)
 
 
+def test_two_streams_own_workspaces():
+    # two decode batches in flight at once on two streams, each with its own
+    # workspace (the pattern of a pipelined caller): neither disturbs the other
+    import torch
+    import attention_head_sinks_gb300 as sa
+    cs = [W.index_case(16, 128, 576, 512, 6000, 2048, cnt, (-2.2, 2.49), NULL, 3700 + i, "s%d" % i)
+          for i, cnt in enumerate(((2048, 7, 600), (1, 1500, 256, 2048)))]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    ins = [(dev(c.q), dev(c.kv), dev(c.indices), dev(c.sinks)) for c in cs]
+    wss = [torch.empty(sa.sa_sparse_index_workspace_size(16, 128, 512, 2048), dtype=torch.uint8,
+                       device="cuda") for _ in cs]
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(3):
+        for k in range(2):
+            with torch.cuda.stream(streams[k]):
+                q, kv, idx, s = ins[k]
+                o = sa.sa_sparse_index_fwd(q, kv, idx, 512, s, NULL, cs[k].scale, workspace=wss[k])
+                if rep == 2:
+                    outs.append(o)
+    torch.cuda.synchronize()
+    for c, (out, lse) in zip(cs, outs):
+        ro, rl, _ = O.sparse_index_fwd(c.q, c.kv, c.indices, c.dv, c.sinks, NULL, c.scale)
+        rel, dl = compare(out, lse, ro, rl)
+        assert rel <= REL_L2_TOL and dl <= LSE_TOL, (c.name, rel, dl)
+
+
 @pytest.mark.parametrize("nq", [600, 1100])
 def test_many_queries(nq):
     # more than 256 queries: each CTA's item lookup scans several queries
