@@ -157,6 +157,30 @@ def test_zero_key0_sink_is_bitwise_no_sink():
     assert torch.equal(l0, l1)
 
 
+def test_key0_extreme_sinks_and_dominant_first_key():
+    # every document's first key carries the largest raw logit of its rows
+    # (q = 4 e0, that key 8 e0, other keys random), with KEY0_BIAS sinks
+    # -inf, -30, +4 and 0 over the four query heads of each KV head: the first
+    # key removed (documents of one token become empty rows), far below the
+    # rest, dominant, or unbiased
+    c = W.block_case(2, 512, 16, 4, 128, 64, 5, 40, (-2.2, 2.49), KEY0, seed=4500,
+                     name="k0_extremes")
+    q = (c.q.astype(np.uint32) << 16).view(np.float32).copy()
+    q[:] = 0.0
+    q[:, :, 0] = 4.0
+    k = (c.k.astype(np.uint32) << 16).view(np.float32).copy()
+    firsts = np.unique(c.cu_docs[:-1])
+    k[firsts, :, :] = 0.0
+    k[firsts, :, 0] = 8.0
+    c.q = W.f32_to_bf16_bits(q)
+    c.k = W.f32_to_bf16_bits(k)
+    sinks = np.tile(np.array([-np.inf, -30.0, 4.0, 0.0], np.float32), 4)
+    out, lse = gpu_run(c, KEY0, sinks=sinks)
+    ro, rl = oracle_run(c, KEY0, sinks=sinks)
+    rel, dl = compare(out, lse, ro, rl)
+    assert rel <= REL_L2_TOL and dl <= LSE_TOL, (rel, dl)
+
+
 @pytest.mark.parametrize("docs_per_row", [200, 300])
 @pytest.mark.parametrize("mode", [NULL, KEY0])
 def test_many_documents(docs_per_row, mode):
