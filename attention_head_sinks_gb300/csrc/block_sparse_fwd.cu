@@ -22,7 +22,9 @@
 // to an ascending list, with a per-block bitmask of the tokens that chose it.
 // The loop walks that list two 64-key blocks per step:
 //   S_j = Q K_j^T (N = 128) into one of two TMEM buffers,
-//   softmax over S_j with per-element selection / causal / document masks,
+//   softmax over S_j with per-element selection / causal / document masks
+//   (a KEY0_BIAS sink is first added to the document's first-key logit in
+//   S_j itself, so the softmax has no sink term),
 //   P_j (bf16) written over S_j, O += P_j V_j with P_j read from TMEM.
 // Persistent: one CTA per SM walks tiles blockIdx.x + n * gridDim.x.
 // Warp roles: warp 2 allocates TMEM, then builds each tile's metadata (token

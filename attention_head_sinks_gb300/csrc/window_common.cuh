@@ -1,7 +1,7 @@
 // window_common.cuh -- per-row pieces of the sliding-window forward shared by
-// both window kernels: row metadata from cu_seqlens, the two-pass softmax
-// over S in tensor memory (P written back as bf16), and the epilogue with the
-// NULL_LOGIT fold.
+// both window kernels: row metadata from cu_seqlens, the KEY0_BIAS sink added
+// to S in tensor memory, the two-pass softmax over S (P written back as
+// bf16), and the epilogue with the NULL_LOGIT fold.
 //
 // Operation: vLLM pull 49815 "[Bugfix][MiMo] Apply vision attention sinks in
 // the window attention path" (KEY0_BIAS on each sequence's first key, which
