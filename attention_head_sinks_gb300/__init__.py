@@ -8,8 +8,7 @@ missing library raises.
 """
 from __future__ import annotations
 
-from ._lib import SAError, lib  # noqa: F401
-from .workloads import SINK_KEY0_BIAS, SINK_NONE, SINK_NULL_LOGIT  # noqa: F401
+from ._lib import SINK_KEY0_BIAS, SINK_NONE, SINK_NULL_LOGIT, SAError, lib  # noqa: F401
 
 __all__ = ["sa_varlen_window_fwd", "sa_sparse_index_fwd", "sa_sparse_index_fwd_fp8",
            "sa_block_sparse_fwd", "sa_block_sparse_fwd_index_heads", "sa_block_select",

@@ -13,6 +13,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libsa.so")
 
 SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_WORKSPACE = range(5)
+# sa_sink_mode values of include/sa.h
+SINK_NONE, SINK_KEY0_BIAS, SINK_NULL_LOGIT = 0, 1, 2
 STATUS_NAMES = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_UNSUPPORTED",
                 3: "SA_ERR_CUDA", 4: "SA_ERR_WORKSPACE"}
 

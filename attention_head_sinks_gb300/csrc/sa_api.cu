@@ -45,9 +45,44 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
 constexpr int kMaxDevices = 64;
-std::atomic<uint32_t*> g_err_ptr[kMaxDevices];
+// Device address of the error word per device, with the id of the context it
+// was looked up in.
+struct ErrSlot {
+  uint64_t ctx;
+  uint32_t* ptr;
+};
+std::mutex g_err_mu;
+ErrSlot g_err_slot[kMaxDevices];
 }  // namespace
+
+uint64_t current_context_id() {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c ||
+      get_id(c, &id) != CUDA_SUCCESS)
+    return 0;
+  return (uint64_t)id;
+}
 
 sa_status fail(sa_status st, const char* fmt, ...) {
   va_list ap;
@@ -159,13 +194,15 @@ uint32_t* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return nullptr;
-  uint32_t* p = g_err_ptr[dev].load(std::memory_order_acquire);
-  if (p) return p;
+  const uint64_t ctx = current_context_id();  // 0 before the runtime made one
+  std::lock_guard<std::mutex> guard(g_err_mu);
+  ErrSlot& slot = g_err_slot[dev];
+  if (slot.ptr && ctx != 0 && slot.ctx == ctx) return slot.ptr;
   void* addr = nullptr;
   if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return nullptr;
-  p = static_cast<uint32_t*>(addr);
-  g_err_ptr[dev].store(p, std::memory_order_release);
-  return p;
+  slot.ctx = current_context_id();
+  slot.ptr = static_cast<uint32_t*>(addr);
+  return slot.ptr;
 }
 
 int num_sms() {
@@ -421,14 +458,19 @@ size_t sa_sparse_index_workspace_size(int32_t num_queries, int32_t num_q_heads,
   return sa::sparse_index_workspace_bytes(num_queries, num_q_heads, topk);
 }
 
-namespace {
-// Shared checks and dispatch of the bf16 and fp8 latent-cache entry points.
+}  // extern "C"
+
+namespace sa {
+// Shared checks and dispatch of the bf16 and fp8 latent-cache entry points
+// and of the allocation-free one (fixed != null: its scratch replaces the
+// workspace once every argument check has passed).
 sa_status sparse_index_entry(const char* fn, const void* q, const void* kv_latent,
                              const float* kv_scale, bool fp8, int64_t num_kv, int32_t dqk,
                              int32_t dv, const int32_t* indices, int32_t topk,
                              int32_t num_queries, int32_t num_q_heads, const float* sinks,
                              int32_t sink_mode, float softmax_scale, void* out, float* lse,
-                             void* workspace, size_t workspace_bytes, void* stream) {
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             const FixedScratch* fixed) {
   if (!q || !kv_latent || !indices || !out || !lse || (fp8 && !kv_scale))
     return fail(SA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
   if (sink_mode < SA_SINK_NONE || sink_mode > SA_SINK_NULL_LOGIT)
@@ -453,11 +495,25 @@ sa_status sparse_index_entry(const char* fn, const void* q, const void* kv_laten
     return fail(SA_ERR_UNSUPPORTED, "%s: num_kv %lld >= 2^31", fn, (long long)num_kv);
   if (topk > sa::sparse_index_max_topk())
     return fail(SA_ERR_UNSUPPORTED, "%s: topk %d > %d", fn, topk, sa::sparse_index_max_topk());
-  if (num_queries > 0 && dqk == 576 && dv == 512) {
+  if (dqk != 576 || dv != 512)
+    return fail(SA_ERR_UNSUPPORTED, "%s: dqk %d / dv %d (supported: 576 / 512)", fn, dqk, dv);
+  if (num_queries > 0) {
     const size_t need = sa::sparse_index_workspace_bytes(num_queries, num_q_heads, topk);
-    if (need > 0 && (!workspace || workspace_bytes < need))
+    if (fixed) {
+      if (need > fixed->bytes)
+        return fail(SA_ERR_UNSUPPORTED,
+                    "%s: these sizes need %zu bytes of scratch, above the fixed %zu bytes "
+                    "(%zu MiB) of this entry point; use sa_sparse_index_fwd with a workspace",
+                    fn, need, fixed->bytes, fixed->bytes >> 20);
+      if (need > 0) {
+        const sa_status st = fixed->address(fn, &workspace);
+        if (st != SA_OK) return st;
+        workspace_bytes = fixed->bytes;
+      }
+    } else if (need > 0 && (!workspace || workspace_bytes < need)) {
       return fail(SA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
                   workspace ? workspace_bytes : (size_t)0);
+    }
   }
   if (num_queries == 0) return SA_OK;
   if (!sa::device_error_word())
@@ -485,7 +541,9 @@ sa_status sparse_index_entry(const char* fn, const void* q, const void* kv_laten
   a.stream = static_cast<cudaStream_t>(stream);
   return sa::launch_sparse_index_fwd(a);
 }
-}  // namespace
+}  // namespace sa
+
+extern "C" {
 
 sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent, int64_t num_kv,
                               int32_t dqk, int32_t dv, const int32_t* indices,
@@ -493,9 +551,10 @@ sa_status sa_sparse_index_fwd(const void* q, const void* kv_latent, int64_t num_
                               const float* sinks, int32_t sink_mode, float softmax_scale,
                               void* out, float* lse, void* workspace,
                               size_t workspace_bytes, void* stream) {
-  return sparse_index_entry("sa_sparse_index_fwd", q, kv_latent, nullptr, false, num_kv, dqk,
-                            dv, indices, topk, num_queries, num_q_heads, sinks, sink_mode,
-                            softmax_scale, out, lse, workspace, workspace_bytes, stream);
+  return sa::sparse_index_entry("sa_sparse_index_fwd", q, kv_latent, nullptr, false, num_kv,
+                                dqk, dv, indices, topk, num_queries, num_q_heads, sinks,
+                                sink_mode, softmax_scale, out, lse, workspace, workspace_bytes,
+                                stream, nullptr);
 }
 
 sa_status sa_sparse_index_fwd_fp8(const void* q, const void* kv_fp8, const float* kv_scale,
@@ -504,9 +563,10 @@ sa_status sa_sparse_index_fwd_fp8(const void* q, const void* kv_fp8, const float
                                   int32_t num_q_heads, const float* sinks, int32_t sink_mode,
                                   float softmax_scale, void* out, float* lse, void* workspace,
                                   size_t workspace_bytes, void* stream) {
-  return sparse_index_entry("sa_sparse_index_fwd_fp8", q, kv_fp8, kv_scale, true, num_kv, dqk,
-                            dv, indices, topk, num_queries, num_q_heads, sinks, sink_mode,
-                            softmax_scale, out, lse, workspace, workspace_bytes, stream);
+  return sa::sparse_index_entry("sa_sparse_index_fwd_fp8", q, kv_fp8, kv_scale, true, num_kv,
+                                dqk, dv, indices, topk, num_queries, num_q_heads, sinks,
+                                sink_mode, softmax_scale, out, lse, workspace, workspace_bytes,
+                                stream, nullptr);
 }
 
 sa_status sa_merge_attn_states(const void* out_a, const float* lse_a, const void* out_b,

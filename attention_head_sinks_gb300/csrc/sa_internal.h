@@ -105,6 +105,28 @@ struct IndexArgs {
   cudaStream_t stream;
 };
 
+// Id of the current CUDA context (unique for the life of the process; a
+// context destroyed and re-created gets a new one), or 0 if none is current.
+uint64_t current_context_id();
+
+// A fixed device array used in place of a caller workspace: its size, and a
+// function that returns its device address on the current device (or a
+// status with a message naming `fn`).
+struct FixedScratch {
+  size_t bytes;
+  sa_status (*address)(const char* fn, void** ptr);
+};
+
+// Checks and dispatch shared by the sparse-index entry points; with `fixed`
+// set, its array serves as the workspace once every argument check passed.
+sa_status sparse_index_entry(const char* fn, const void* q, const void* kv_latent,
+                             const float* kv_scale, bool fp8, int64_t num_kv, int32_t dqk,
+                             int32_t dv, const int32_t* indices, int32_t topk,
+                             int32_t num_queries, int32_t num_q_heads, const float* sinks,
+                             int32_t sink_mode, float softmax_scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             const FixedScratch* fixed);
+
 size_t sparse_index_workspace_bytes(int32_t num_queries, int32_t num_q_heads, int32_t topk);
 int sparse_index_max_topk();
 sa_status launch_sparse_index_fwd(const IndexArgs& a);

@@ -47,7 +47,7 @@
 #include <math.h>
 
 #include <algorithm>
-#include <atomic>
+#include <mutex>
 #include <utility>
 
 #include "sa_internal.h"
@@ -1281,22 +1281,59 @@ sa_status launch_sparse_index_fwd(const IndexArgs& a) {
 // Some callers cannot obtain device memory for a workspace: code embedded in a
 // host runtime that owns the whole device memory pool and hands its plugins no
 // allocator, or a serving loop that forbids any allocation once it is running.
-// sa_sparse_index_fwd_noalloc serves them by keeping the split-KV partials in
+// sa_sparse_index_fwd_noalloc serves them by keeping the split-KV scratch in
 // the fixed array below instead of a caller workspace.  The array is reserved
 // on every GPU that loads this library and stays reserved until the process
-// exits.  Every call shares it and it keeps the last call's contents; nothing
-// in it has to start at zero, because each call writes every (m, l) entry and
-// every partial row it later reads.  Two calls whose work overlaps on the GPU
-// (different streams, or different host threads) race on the array.
+// exits.  Every call shares it and it keeps the last call's contents; each
+// call writes every entry it later reads, so nothing in it has to start at
+// zero.  Two calls whose work overlaps on the GPU (different streams, or
+// different host threads) race on the array.
 namespace sa {
 namespace {
 constexpr size_t kNoAllocScratchBytes = (size_t)64 << 20;  // 64 MiB
 constexpr int kNoAllocMaxDevices = 64;
-std::atomic<void*> g_noalloc_scratch_ptr[kNoAllocMaxDevices];
+
+// The array's device address per device, with the id of the context it was
+// looked up in: a context destroyed and re-created (cudaDeviceReset) may
+// place the array elsewhere, and gets a new id, so the address is looked up
+// again in it.
+struct NoAllocSlot {
+  uint64_t ctx;
+  void* ptr;
+};
+std::mutex g_noalloc_mu;
+NoAllocSlot g_noalloc_slot[kNoAllocMaxDevices];
 }  // namespace
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+namespace {
+// Set-up, once per device and context, with that device current: the
+// host-side name of the array is not a device address, so the runtime is
+// asked for it.
+sa_status noalloc_scratch_address(const char* fn, void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(SA_ERR_CUDA, "%s: no usable CUDA device", fn);
+  const uint64_t ctx = current_context_id();
+  std::lock_guard<std::mutex> guard(g_noalloc_mu);
+  NoAllocSlot& slot = g_noalloc_slot[dev];
+  if (slot.ptr && ctx != 0 && slot.ctx == ctx) {
+    *out = slot.ptr;
+    return SA_OK;
+  }
+  void* ptr = nullptr;
+  e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess || !ptr)
+    return fail(SA_ERR_CUDA, "%s: cudaGetSymbolAddress of the scratch array failed: %s", fn,
+                cudaGetErrorString(e));
+  slot.ctx = current_context_id();
+  slot.ptr = ptr;
+  *out = ptr;
+  return SA_OK;
+}
+}  // namespace
 }  // namespace sa
 
 extern "C" sa_status sa_sparse_index_fwd_noalloc(
@@ -1304,28 +1341,8 @@ extern "C" sa_status sa_sparse_index_fwd_noalloc(
     const int32_t* indices, int32_t topk, int32_t num_queries, int32_t num_q_heads,
     const float* sinks, int32_t sink_mode, float softmax_scale, void* out, float* lse,
     void* stream) {
-  const char* fn = "sa_sparse_index_fwd_noalloc";
-  const size_t need = sa_sparse_index_workspace_size(num_queries, num_q_heads, dv, topk);
-  if (need > sa::kNoAllocScratchBytes)
-    return sa::fail(SA_ERR_UNSUPPORTED,
-                    "%s: these sizes need %zu bytes of scratch, above the fixed %zu bytes "
-                    "(64 MiB) of this entry point; use sa_sparse_index_fwd with a workspace",
-                    fn, need, sa::kNoAllocScratchBytes);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= sa::kNoAllocMaxDevices)
-    return sa::fail(SA_ERR_CUDA, "%s: no usable CUDA device", fn);
-  void* ptr = sa::g_noalloc_scratch_ptr[dev].load(std::memory_order_acquire);
-  if (!ptr) {
-    // One-time set-up on this device (the device is current): the host-side
-    // name of the array is not a device address, so ask the runtime for it.
-    e = cudaGetSymbolAddress(&ptr, sa::g_noalloc_scratch);
-    if (e != cudaSuccess || !ptr)
-      return sa::fail(SA_ERR_CUDA, "%s: cudaGetSymbolAddress failed: %s", fn,
-                      cudaGetErrorString(e));
-    sa::g_noalloc_scratch_ptr[dev].store(ptr, std::memory_order_release);
-  }
-  return sa_sparse_index_fwd(q, kv_latent, num_kv, dqk, dv, indices, topk, num_queries,
-                             num_q_heads, sinks, sink_mode, softmax_scale, out, lse, ptr,
-                             sa::kNoAllocScratchBytes, stream);
+  static const sa::FixedScratch fixed = {sa::kNoAllocScratchBytes, sa::noalloc_scratch_address};
+  return sa::sparse_index_entry("sa_sparse_index_fwd_noalloc", q, kv_latent, nullptr, false,
+                                num_kv, dqk, dv, indices, topk, num_queries, num_q_heads, sinks,
+                                sink_mode, softmax_scale, out, lse, nullptr, 0, stream, &fixed);
 }

@@ -28,7 +28,7 @@ import math
 
 import numpy as np
 
-SINK_NONE, SINK_KEY0_BIAS, SINK_NULL_LOGIT = 0, 1, 2
+from ._lib import SINK_KEY0_BIAS, SINK_NONE, SINK_NULL_LOGIT  # noqa: F401
 
 
 def _rng(seed: int) -> np.random.Generator:

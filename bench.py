@@ -57,6 +57,15 @@ def _torch_bits(a):
     return W.to_torch(a)
 
 
+def _obufs(runner):
+    """Output arrays the oracle keeps between the sampled calls of one
+    runner, so that a sampled call does not allocate and fill full-size
+    outputs (the arithmetic is the oracle's, unchanged)."""
+    if not hasattr(runner, "_oracle_bufs"):
+        runner._oracle_bufs = {}
+    return runner._oracle_bufs
+
+
 # ----------------------------------------------------------------------------
 # workloads: inputs, algorithmic bytes / flops, the call, the oracle sample
 # ----------------------------------------------------------------------------
@@ -80,6 +89,10 @@ class WindowRunner:
             self.c = W.vision_window(16384, W.SINK_KEY0_BIAS)
         elif name == "vision_window_4096tok":
             self.c = W.vision_window(4096, W.SINK_KEY0_BIAS)
+        elif name == "tiny_window_128tok":
+            # launch-bound parity case: its inputs stay L2-resident
+            self.bound = "launch"
+            self.c = W.tiny_window(W.SINK_KEY0_BIAS)
         else:
             self.c = W.gqa_window(W.SINK_KEY0_BIAS)
         self.mode = self.c.mode
@@ -157,7 +170,7 @@ class WindowRunner:
         from oracle import sa_oracle
         c = self.c
         sa_oracle.window_fwd(c.q, c.k, c.v, c.cu_seqlens, c.window_left,
-                             c.window_right, c.sinks, self.mode, c.scale, rows=rows)
+                             c.window_right, c.sinks, self.mode, c.scale, rows=rows, bufs=_obufs(self))
 
 
 class IndexRunner:
@@ -253,7 +266,7 @@ class IndexRunner:
         from oracle import sa_oracle
         c = self.c
         sa_oracle.sparse_index_fwd(c.q, c.kv, c.indices, c.dv, c.sinks, self.mode,
-                                   c.scale, rows=rows)
+                                   c.scale, rows=rows, bufs=_obufs(self))
 
 
 class IndexFp8Runner(IndexRunner):
@@ -342,7 +355,7 @@ class IndexFp8Runner(IndexRunner):
         from oracle import sa_oracle
         c = self.c
         sa_oracle.sparse_index_fwd_fp8(c.q, c.kv, c.kv_scale, c.indices, c.dv, c.sinks,
-                                       self.mode, c.scale, rows=rows)
+                                       self.mode, c.scale, rows=rows, bufs=_obufs(self))
 
 
 class BlockRunner:
@@ -437,7 +450,7 @@ class BlockRunner:
         c = self.c
         sa_oracle.block_sparse_fwd(c.q, c.k, c.v, c.batch, c.seq_len, c.block_table,
                                    c.block_size, c.cu_docs, c.sinks, self.mode,
-                                   c.scale, rows=rows)
+                                   c.scale, rows=rows, bufs=_obufs(self))
 
 
 class MergeRunner:
@@ -591,7 +604,7 @@ class SelectRunner:
         from oracle import sa_oracle
         c = self.c
         sa_oracle.block_select(c.index_q, c.index_k, c.batch, c.seq_len, c.block_size, c.topk,
-                               rows=rows)
+                               rows=rows, bufs=_obufs(self))
 
 
 class SelectedBlockRunner(BlockRunner):
@@ -677,13 +690,14 @@ class SelectedBlockRunner(BlockRunner):
         from oracle import sa_oracle
         c, sc = self.c, self.sc
         tabs, _ = sa_oracle.block_select(sc.index_q, sc.index_k, sc.batch, sc.seq_len,
-                                         sc.block_size, sc.topk, rows=rows)
+                                         sc.block_size, sc.topk, rows=rows, bufs=_obufs(self))
         sa_oracle.block_sparse_fwd_index_heads(c.q, c.k, c.v, c.batch, c.seq_len, tabs,
                                                c.block_size, c.cu_docs, c.sinks, self.mode,
-                                               c.scale, rows=rows)
+                                               c.scale, rows=rows, bufs=_obufs(self))
 
 
 RUNNERS = {
+    "tiny_window_128tok": WindowRunner,
     "vision_window_16384tok": WindowRunner,
     "vision_window_4096tok": WindowRunner,
     "gqa_window_16384tok": WindowRunner,
@@ -701,7 +715,12 @@ RUNNERS = {
 # measurement helpers
 # ----------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 100 ms while it runs: SM clock, power, GPU
+    utilisation and the throttle reasons.  A sample counts as under load when
+    the GPU reports at least 50 % utilisation; the SM clock median is taken
+    over those samples."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
@@ -727,23 +746,38 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
+        sm, smax, load_sm, power, reasons = [], [], [], [], set()
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                clk, cmax = float(f[1]), float(f[2])
             except ValueError:
                 continue
-            for name, val in zip(self.REASONS, f[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
+            sm.append(clk)
+            smax.append(cmax)
+            try:
+                util = float(f[4])
+            except ValueError:
+                util = 0.0
+            if util >= 50.0:
+                load_sm.append(clk)
+                try:
+                    power.append(float(f[3]))
+                except ValueError:
+                    pass
+                # throttle reasons count while the GPU works
+                for name, val in zip(self.REASONS, f[6:10]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(load_sm) if load_sm else None,
+                "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "samples_under_load": len(load_sm),
+                "sm_mhz_min_under_load": min(load_sm) if load_sm else None,
+                "power_w_median_under_load": statistics.median(power) if power else None}
 
 
 def gpu_uuid():
@@ -764,9 +798,32 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def kernel_sources(path):
+    """The kernel file and every local header it includes (transitively,
+    ``#include "..."``), the file first and the headers in path order."""
+    import re
+    seen, todo, heads = set(), [os.path.join(ROOT, path)], []
+    while todo:
+        f = os.path.normpath(todo.pop())
+        if f in seen or not os.path.exists(f):
+            continue
+        seen.add(f)
+        if f != os.path.normpath(os.path.join(ROOT, path)):
+            heads.append(f)
+        for inc in re.findall(r'^\s*#\s*include\s+"([^"]+)"', open(f).read(), re.M):
+            todo.append(os.path.join(os.path.dirname(f), inc))
+    return [os.path.normpath(os.path.join(ROOT, path))] + sorted(heads)
+
+
 def kernel_source_hash(path):
-    with open(os.path.join(ROOT, path), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:12]
+    """Hash of the kernel file together with the local headers it includes,
+    so that a change in a shared header also invalidates recorded traffic."""
+    h = hashlib.sha256()
+    for f in kernel_sources(path):
+        h.update(os.path.relpath(f, ROOT).encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
 
 
 def recorded_traffic(workload, src_hash):
@@ -836,10 +893,30 @@ def cpu_baseline(runner, budget_s=10.0):
                       "scaled to one call" % (n, total, len(spans), runner.oracle_kind)}
 
 
+def arm_config(runner, world):
+    """The ``config`` object of a bench line (both arms): the workload's own
+    keys, the job layout and the L2 hygiene of the timed region."""
+    cfg = runner.config()
+    nsets = input_sets(runner)
+    if getattr(runner, "bound", "") == "launch":
+        l2 = ("%d rotating input sets (%.1f MB touched), L2-resident: a launch-bound "
+              "parity case" % (nsets, nsets * runner.touched_bytes() / 1e6))
+    else:
+        l2 = ("%d rotating input sets (%.0f MB touched) > 129 MB L2" %
+              (nsets, nsets * runner.touched_bytes() / 1e6))
+    cfg.update({"global_batch": world, "parallelism": "replicas x%d" % world, "l2": l2})
+    return cfg
+
+
+def input_sets(runner):
+    """Input sets rotated between calls so that every call touches more than
+    L2 since the last use of its set (at most 64 sets)."""
+    return int(min(64, max(2, -(-3 * L2_BYTES // runner.touched_bytes()))))
+
+
 def run_reference(args, rank):
     if rank != 0:
         return
-    from oracle import sa_oracle
     runner = RUNNERS[args.workload](args.workload)
     total = runner.oracle_rows()
     per = max(1, total // 128)           # each step: 1/128 of the call's rows
@@ -857,7 +934,7 @@ def run_reference(args, rank):
         "unit": "us/call", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / max(args.steps, 1), 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic", "config": runner.config(),
+        "dtype": "f64", "data": "synthetic", "config": arm_config(runner, args.gpus),
         "cpu_baseline": {"value": round(us_call, 1), "unit": "us/call",
                          "cores": runner.oracle_cores(), "kind": "oracle",
                          "sample": "each step %d of %d query rows (all heads), walking "
@@ -870,6 +947,201 @@ def run_reference(args, rank):
 
 
 # ----------------------------------------------------------------------------
+# the default run also measures every other configuration of the workload set
+# (and the two composite steps), each on its own inputs; windows and decodes
+# with these many calls, the prefills with fewer
+EXTRA_WORKLOADS = [
+    ("tiny_window_128tok", 2000),
+    ("vision_window_4096tok", 2000),
+    ("gqa_window_16384tok", 1000),
+    ("mla_sparse_decode", 1000),
+    ("mla_sparse_decode_fp8", 1000),
+    ("dsa_block_prefill", 100),
+    ("dsa_block_prefill_selected", 100),
+]
+SUSTAINED_S = 1.5
+
+
+class Bench:
+    """Measurement of one workload on this rank (CUDA events on the launching
+    stream, max over ranks)."""
+
+    def __init__(self, runner, dist, world):
+        import torch
+        self.torch = torch
+        self.r = runner
+        self.dist = dist
+        self.world = world
+        self.nbytes, self.flops = runner.counts()
+        self.nsets = input_sets(runner)
+        runner.setup(self.nsets)
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+        self.torch.cuda.synchronize()
+
+    def warm(self, n):
+        for i in range(n):
+            self.r.call(i)
+        self.barrier()
+
+    def timed(self, mode, steps):
+        """The contract's timed region: ``steps`` calls through the public
+        API, bracketed by barrier + synchronize, CUDA events on the launching
+        stream at both ends; nothing else is enqueued in between.  Returns
+        the slowest rank's milliseconds."""
+        torch = self.torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.barrier()
+        e0.record()
+        for i in range(steps):
+            self.r.call(i, mode)
+        e1.record()
+        self.barrier()
+        return max_over_ranks(e0.elapsed_time(e1), self.dist, "cuda")
+
+    def device_times(self, mode, steps):
+        """Device time of each call (CUDA events around it on the launching
+        stream), with the calls queued behind a device-side sleep so that the
+        host's enqueue time never appears as idle time between the events."""
+        torch = self.torch
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        self.barrier()
+        sleep = getattr(torch.cuda, "_sleep", None)
+        if sleep is not None:  # about 60 us of host time per queued call
+            sleep(int(2.0e9 * (0.005 + steps * 60e-6)))
+        for i in range(steps):
+            starts[i].record()
+            self.r.call(i, mode)
+            ends[i].record()
+        self.barrier()
+        return [s_.elapsed_time(e_) * 1000.0 for s_, e_ in zip(starts, ends)]
+
+    def sink_cost(self, steps):
+        """Timed regions of back-to-back calls in the workload's mode and with
+        sinks disabled, in alternating rounds so that a drift in clocks or in
+        the machine's other load falls on both alike; and the medians of
+        isolated launches of both modes, alternating in the same way."""
+        rounds = 4
+        per_round = max(steps // rounds, 10)
+        t_mode = t_none = 0.0
+        for _ in range(rounds):
+            t_mode += self.timed(self.r.mode, per_round)
+            t_none += self.timed(W.SINK_NONE, per_round)
+        ndev = max(min(steps, 500), 10)
+        chunk = min(ndev, 50)
+        per, per_none = [], []
+        for _ in range((ndev + chunk - 1) // chunk):
+            per += self.device_times(self.r.mode, chunk)
+            per_none += self.device_times(W.SINK_NONE, chunk)
+        kern, kern_none = statistics.median(per), statistics.median(per_none)
+        return {"sink_cost": round(t_mode / t_none - 1.0, 4),
+                "sink_cost_isolated": round(kern / kern_none - 1.0, 4),
+                "launch_us_isolated": round(kern, 3),
+                "launch_us_isolated_sinks_disabled": round(kern_none, 3)}
+
+    def e2e(self, steps):
+        """End to end through the public API: pinned host inputs -> device,
+        the call, results -> host, each step on one of two streams in turn
+        (its own device buffers), so that one step's copies overlap the other
+        step's call and the copies in the other direction."""
+        torch = self.torch
+        nslot = 2
+        ios = [self.r.host_io(k) for k in range(nslot)]
+        host_in = [h.pin_memory() for h in ios[0][0]]
+        dev_in = [[torch.empty_like(h, device="cuda") for h in host_in] for _ in range(nslot)]
+        host_out = [[torch.empty_like(o, device="cpu").pin_memory() for o in io[1]]
+                    for io in ios]
+        streams = [torch.cuda.Stream() for _ in range(nslot)]
+
+        def step(i):
+            k = i % nslot
+            with torch.cuda.stream(streams[k]):
+                for d_, h_ in zip(dev_in[k], host_in):
+                    d_.copy_(h_, non_blocking=True)
+                ios[k][2](dev_in[k])
+                for h_, o_ in zip(host_out[k], ios[k][1]):
+                    h_.copy_(o_, non_blocking=True)
+
+        for i in range(2 * nslot):
+            step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream()
+        self.barrier()
+        e0.record(cur)
+        for s_ in streams:
+            s_.wait_event(e0)
+        for i in range(steps):
+            step(i)
+        for s_ in streams:
+            cur.wait_stream(s_)
+        e1.record(cur)
+        self.barrier()
+        ms = max_over_ranks(e0.elapsed_time(e1), self.dist, "cuda")
+        h2d = sum(h.numel() * h.element_size() for h in host_in)
+        d2h = sum(h.numel() * h.element_size() for h in host_out[0])
+        return {"value": round(ms * 1000.0 / steps / self.world, 2), "unit": "us/call",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    def sustained(self, seconds):
+        """Back-to-back calls for about ``seconds`` (a count taken from a
+        short probe), timed as one region: the per-call time with the GPU
+        held busy long enough for its clocks and power to settle."""
+        probe = max(self.timed(self.r.mode, 200) / 200.0, 1e-3)
+        n = int(max(200, seconds * 1e3 / probe))
+        ms = self.timed(self.r.mode, n)
+        return {"value": round(ms * 1000.0 / n / self.world, 3), "unit": "us/call",
+                "calls": n, "seconds": round(ms / 1000.0, 3)}
+
+    def roofline(self, call_us, traffic, src_hash):
+        hbm_peak, tf_peak, peak_src = measured_peaks()
+        gbs = self.nbytes / (call_us * 1e-6) / 1e9
+        tfs = self.flops / (call_us * 1e-6) / 1e12
+        if self.r.bound == "tensor":
+            roof = {"bound": "tensor", "achieved": round(tfs, 1), "peak": tf_peak,
+                    "unit": "TFLOP/s", "frac": round(tfs / tf_peak, 4), "traffic": traffic}
+            other = {"alg_gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm_peak, 4)}
+        else:
+            roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                    "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": traffic}
+            other = {"alg_tflops": round(tfs, 2),
+                     "frac_of_bf16_peak": round(tfs / tf_peak, 4)}
+        roof.update({"peak_source": peak_src, "alg_bytes": self.nbytes,
+                     "alg_flops": self.flops, "call_us": round(call_us, 3),
+                     "source_hash": src_hash})
+        return roof, other
+
+
+def workload_entry(name, steps, dist, world, e2e_steps):
+    """One configuration of the workload set, measured with the contract's
+    rules on its own inputs: its per-call time and roofline, sink cost,
+    isolated launch and end-to-end time."""
+    import torch
+    runner = RUNNERS[name](name)
+    b = Bench(runner, dist, world)
+    b.warm(max(10, steps // 10))
+    ms = b.timed(runner.mode, steps)
+    call_us = ms * 1000.0 / steps
+    src_hash = kernel_source_hash(runner.source)
+    roof, other = b.roofline(call_us, recorded_traffic(name, src_hash), src_hash)
+    sc = b.sink_cost(max(steps // 2, 40))
+    roof["launch_us_isolated"] = sc.pop("launch_us_isolated")
+    entry = {"value": round(call_us / world, 3), "unit": "us/call", "steps": steps,
+             "roofline": roof, "secondary": other, "e2e": b.e2e(max(10, e2e_steps // 2)),
+             "gpu_launches": steps * runner.launches_per_call(),
+             "config": arm_config(runner, world)}
+    entry.update(sc)
+    if name in PAGES_H100_US:
+        entry["vs_pages_h100"] = round(entry["value"] / PAGES_H100_US[name], 4)
+    del b, runner
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -878,6 +1150,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="vision_window_16384tok", choices=sorted(RUNNERS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="measure only --workload (no per-configuration entries)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -898,115 +1172,34 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-
     runner = RUNNERS[args.workload](args.workload)
-    nbytes, flops = runner.counts()
-    nsets = max(2, -(-3 * L2_BYTES // runner.touched_bytes()))
-    runner.setup(nsets)
-
-    for i in range(args.warmup):
-        runner.call(i)
-    barrier()
-
-    def timed(mode, steps):
-        """The contract's timed region: K calls through the public API,
-        bracketed by barrier + synchronize, CUDA events on the launching
-        stream at both ends.  Nothing else is enqueued in between."""
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        e0.record()
-        for i in range(steps):
-            runner.call(i, mode)
-        e1.record()
-        barrier()
-        return e0.elapsed_time(e1)
-
-    def device_times(mode, steps):
-        """Device time of each call (CUDA events around it on the launching
-        stream), with the calls queued behind a device-side sleep so that the
-        host's enqueue time never appears as idle time between the events."""
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        barrier()
-        sleep = getattr(torch.cuda, "_sleep", None)
-        if sleep is not None:  # about 60 us of host time per queued call
-            sleep(int(2.0e9 * (0.005 + steps * 60e-6)))
-        for i in range(steps):
-            starts[i].record()
-            runner.call(i, mode)
-            ends[i].record()
-        barrier()
-        return [s_.elapsed_time(e_) * 1000.0 for s_, e_ in zip(starts, ends)]
-
+    b = Bench(runner, dist, world)
+    # the clocks are sampled over every timed leg of the run
     sampler = ClockSampler(gpu_uuid())
-    total_ms = timed(runner.mode, args.steps)
-    clocks = sampler.stop()
-    # the sink cost: timed regions of back-to-back calls in the timed mode and
-    # with sinks disabled, in alternating rounds so that a drift in clocks or
-    # in the machine's other load falls on both alike
-    rounds = 4
-    per_round = max(args.steps // rounds, 10)
-    t_mode = t_none = 0.0
-    for _ in range(rounds):
-        t_mode += timed(runner.mode, per_round)
-        t_none += timed(W.SINK_NONE, per_round)
-    # isolated launches of both modes, alternating in the same way
-    ndev = max(min(args.steps, 500), 10)
-    chunk = min(ndev, 50)
-    per, per_none = [], []
-    for _ in range((ndev + chunk - 1) // chunk):
-        per += device_times(runner.mode, chunk)
-        per_none += device_times(W.SINK_NONE, chunk)
-
-    step_ms = max_over_ranks(total_ms / args.steps, dist, "cuda")
-    # per call over the timed region (back-to-back calls, the roofline's
-    # denominator: algorithmic bytes and flops are counted per call), and per
-    # isolated launch (events around each call; medians, the sink-cost
-    # comparison)
+    b.warm(args.warmup)
+    step_ms = b.timed(runner.mode, args.steps) / args.steps
     call_us = step_ms * 1000.0
-    kern_us = statistics.median(per)
-    kern_us_none = statistics.median(per_none)
+    sc = b.sink_cost(args.steps)
+    e2e = b.e2e(args.e2e_steps)
+    sustained = b.sustained(SUSTAINED_S)
 
-    # end to end: pinned host inputs -> device, the call, results -> host, each
-    # step on one of two streams in turn (its own device buffers), so that one
-    # step's copies overlap the other's call and copies in the other direction
-    nslot = 2
-    ios = [runner.host_io(k) for k in range(nslot)]
-    host_in = [h.pin_memory() for h in ios[0][0]]
-    dev_in = [[torch.empty_like(h, device="cuda") for h in host_in] for _ in range(nslot)]
-    host_out = [[torch.empty_like(o, device="cpu").pin_memory() for o in io[1]] for io in ios]
-    streams = [torch.cuda.Stream() for _ in range(nslot)]
+    src_hash = kernel_source_hash(runner.source)
+    traffic = recorded_traffic(args.workload, src_hash)
+    roof, other = b.roofline(call_us, traffic, src_hash)
+    roof["launch_us_isolated"] = sc["launch_us_isolated"]
+    roof["sustained_call_us"] = sustained["value"]
 
-    def e2e_step(i):
-        k = i % nslot
-        with torch.cuda.stream(streams[k]):
-            for d_, h_ in zip(dev_in[k], host_in):
-                d_.copy_(h_, non_blocking=True)
-            ios[k][2](dev_in[k])
-            for h_, o_ in zip(host_out[k], ios[k][1]):
-                h_.copy_(o_, non_blocking=True)
-
-    for i in range(2 * nslot):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    cur = torch.cuda.current_stream()
-    e0.record(cur)
-    for s_ in streams:
-        s_.wait_event(e0)
-    for i in range(args.e2e_steps):
-        e2e_step(i)
-    for s_ in streams:
-        cur.wait_stream(s_)
-    e1.record(cur)
-    torch.cuda.synchronize()
-    e2e_us = e0.elapsed_time(e1) * 1000.0 / args.e2e_steps
-    h2d = sum(h.numel() * h.element_size() for h in host_in)
-    d2h = sum(h.numel() * h.element_size() for h in host_out[0])
+    workloads = {}
+    if not args.no_workloads and args.workload == "vision_window_16384tok":
+        del b
+        torch.cuda.empty_cache()
+        for name, steps in EXTRA_WORKLOADS:
+            try:
+                workloads[name] = workload_entry(name, steps, dist, world, args.e2e_steps)
+            except Exception as exc:  # reported, never hidden
+                workloads[name] = {"error": "%s: %s" % (type(exc).__name__, exc)}
+            log("workload %s: %s" % (name, json.dumps(workloads[name].get("value"))))
+    clocks = sampler.stop()
 
     import attention_head_sinks_gb300 as sa
     err = sa.sa_device_error()
@@ -1016,27 +1209,12 @@ def main():
             dist.destroy_process_group()
         return
 
-    hbm_peak, tf_peak, peak_src = measured_peaks()
-    src_hash = kernel_source_hash(runner.source)
-    traffic = recorded_traffic(args.workload, src_hash)
-    gbs = nbytes / (call_us * 1e-6) / 1e9
-    tfs = flops / (call_us * 1e-6) / 1e12
-    if runner.bound == "hbm":
-        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
-                "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": traffic}
-        other = {"alg_tflops": round(tfs, 2), "frac_of_bf16_peak": round(tfs / tf_peak, 4)}
-    else:
-        roof = {"bound": "tensor", "achieved": round(tfs, 1), "peak": tf_peak,
-                "unit": "TFLOP/s", "frac": round(tfs / tf_peak, 4), "traffic": traffic}
-        other = {"alg_gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm_peak, 4)}
-    roof.update({"peak_source": peak_src, "alg_bytes": nbytes, "alg_flops": flops,
-                 "call_us": round(call_us, 3), "launch_us_isolated": round(kern_us, 3),
-                 "source_hash": src_hash})
     value_us = job_value_us(step_ms, world)
-    cfg = runner.config()
-    cfg.update({"global_batch": world, "parallelism": "replicas x%d" % world,
-                "l2": "%d rotating input sets (%.0f MB touched) > 129 MB L2" %
-                      (nsets, nsets * runner.touched_bytes() / 1e6)})
+    head = {"value": round(value_us, 3), "unit": "us/call", "steps": args.steps,
+            "roofline": roof, "sink_cost": sc["sink_cost"], "e2e": e2e,
+            "gpu_launches": args.steps * runner.launches_per_call()}
+    if workloads:
+        workloads = dict([(args.workload, head)] + list(workloads.items()))
     line = {
         "metric": METRIC,
         "value": round(value_us, 3),
@@ -1051,18 +1229,20 @@ def main():
                         if args.workload in PAGES_H100_US else None),
         "dtype": "bf16",
         "data": "synthetic",
-        "config": cfg,
+        "config": arm_config(runner, world),
         "roofline": roof,
         "secondary": other,
-        "sink_cost": round(t_mode / t_none - 1.0, 4),
-        "sink_cost_isolated": round(kern_us / kern_us_none - 1.0, 4),
-        "launch_us_isolated_sinks_disabled": round(kern_us_none, 3),
-        "e2e": {"value": round(e2e_us, 2), "unit": "us/call",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "sink_cost": sc["sink_cost"],
+        "sink_cost_isolated": sc["sink_cost_isolated"],
+        "launch_us_isolated_sinks_disabled": sc["launch_us_isolated_sinks_disabled"],
+        "sustained": sustained,
+        "e2e": e2e,
         "gpu_launches": args.steps * runner.launches_per_call(),
         "clocks": clocks,
         "device_error": err,
     }
+    if workloads:
+        line["workloads"] = workloads
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(runner)
     print(json.dumps(line), flush=True)

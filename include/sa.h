@@ -292,13 +292,17 @@ SA_API sa_status sa_merge_attn_states(const void* out_a, const float* lse_a,
  * errors are those of sa_sparse_index_fwd, without the workspace.
  *
  * The split-KV scratch is a fixed 64 MiB array inside the library, reserved on
- * every GPU that loads the library until the process exits.  Sizes whose
- * sa_sparse_index_workspace_size() exceeds 64 MiB are rejected with
- * SA_ERR_UNSUPPORTED and a message; use sa_sparse_index_fwd for them.  The
- * call itself allocates nothing.  The first call on each device looks up the
- * array's device address once (make that first call before any stream
- * capture).  All calls share the array: calls whose work overlaps on the GPU
- * (other streams or host threads) race and must be serialised by the caller.
+ * every GPU that loads the library until the process exits.  Every argument
+ * is checked first, as sa_sparse_index_fwd checks it (same statuses, messages
+ * naming this entry point); then sizes whose sa_sparse_index_workspace_size()
+ * exceeds 64 MiB are rejected with SA_ERR_UNSUPPORTED and a message; use
+ * sa_sparse_index_fwd for them.  The call itself allocates nothing.  The first
+ * call on each device looks up the array's device address once (make that
+ * first call before any stream capture); the address is kept with the id of
+ * the CUDA context it belongs to, and looked up again when the device's
+ * context has been destroyed and re-created (cudaDeviceReset).  All calls
+ * share the array: calls whose work overlaps on the GPU (other streams or
+ * host threads) race and must be serialised by the caller.
  */
 SA_API sa_status sa_sparse_index_fwd_noalloc(const void* q, const void* kv_latent,
                                              int64_t num_kv, int32_t dqk, int32_t dv,

@@ -7,7 +7,10 @@ patterns, ``cu_seqlens`` / indices / tables as ``int32``, sinks as ``float32``,
 and returns ``(out, lse, key_count)`` as float64 / float64 / int32 arrays.
 ``rows=(begin, end)`` restricts the work to a slice of query rows (the other
 rows of ``out`` and ``lse`` are NaN), which is how full-size workloads are
-sampled.
+sampled.  ``bufs`` (a dict the caller keeps between calls) lends the output
+arrays: a call finds those of an earlier call with the same shapes there
+instead of allocating and filling full-size outputs each time (rows outside
+``rows`` then hold what an earlier call left).  It changes no arithmetic.
 """
 from __future__ import annotations
 
@@ -61,6 +64,17 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _outputs(bufs, key, specs):
+    """Output arrays for ``specs`` = ((shape, dtype, fill), ...): new ones, or
+    with ``bufs`` the ones made under the same key and shapes before."""
+    if bufs is None:
+        return [np.full(sh, fill, dt) for sh, dt, fill in specs]
+    k = (key,) + tuple((tuple(sh), np.dtype(dt).str) for sh, dt, _ in specs)
+    if k not in bufs:
+        bufs[k] = [np.full(sh, fill, dt) for sh, dt, fill in specs]
+    return bufs[k]
+
+
 def _sinks(sinks, hq):
     if sinks is None:
         return np.zeros(hq, np.float32)
@@ -68,7 +82,7 @@ def _sinks(sinks, hq):
 
 
 def window_fwd(q, k, v, cu_seqlens, window_left, window_right, sinks, mode,
-               scale, rows=None):
+               scale, rows=None, bufs=None):
     """Sliding-window attention over ``cu_seqlens``-packed sequences.
 
     q ``[T,Hq,D]``, k/v ``[T,Hkv,D]`` (uint16 bf16 bits); returns out
@@ -80,9 +94,9 @@ def window_fwd(q, k, v, cu_seqlens, window_left, window_right, sinks, mode,
     hkv = k.shape[1]
     s = _sinks(sinks, hq)
     b, e = (0, T) if rows is None else rows
-    out = np.full((T, hq, d), np.nan)
-    lse = np.full((hq, T), np.nan)
-    cnt = np.full((T, hq), -1, np.int32)
+    out, lse, cnt = _outputs(bufs, "window", (((T, hq, d), np.float64, np.nan),
+                                              ((hq, T), np.float64, np.nan),
+                                              ((T, hq), np.int32, -1)))
     rc = _lib().oracle_window_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, T, hq, hkv, d,
         int(window_left), int(window_right), _ptr(s), int(mode), float(scale),
@@ -92,7 +106,7 @@ def window_fwd(q, k, v, cu_seqlens, window_left, window_right, sinks, mode,
     return out, lse, cnt
 
 
-def sparse_index_fwd(q, kv, indices, dv, sinks, mode, scale, rows=None):
+def sparse_index_fwd(q, kv, indices, dv, sinks, mode, scale, rows=None, bufs=None):
     """Top-k index attention into one shared latent cache.
 
     q ``[Nq,Hq,dqk]``, kv ``[nkv,dqk]`` (uint16 bf16 bits), indices
@@ -105,9 +119,9 @@ def sparse_index_fwd(q, kv, indices, dv, sinks, mode, scale, rows=None):
     topk = idx.shape[1]
     s = _sinks(sinks, hq)
     b, e = (0, nq) if rows is None else rows
-    out = np.full((nq, hq, dv), np.nan)
-    lse = np.full((hq, nq), np.nan)
-    cnt = np.full((nq,), -1, np.int32)
+    out, lse, cnt = _outputs(bufs, "index", (((nq, hq, dv), np.float64, np.nan),
+                                             ((hq, nq), np.float64, np.nan),
+                                             ((nq,), np.int32, -1)))
     rc = _lib().oracle_sparse_index_fwd(
         _ptr(q), _ptr(kv), kv.shape[0], dqk, int(dv), _ptr(idx), topk, nq, hq,
         _ptr(s), int(mode), float(scale), _ptr(out), _ptr(lse), _ptr(cnt), b, e)
@@ -117,7 +131,7 @@ def sparse_index_fwd(q, kv, indices, dv, sinks, mode, scale, rows=None):
 
 
 def block_sparse_fwd(q, k, v, batch, seq_len, block_table, block_size,
-                     cu_docs, sinks, mode, scale, rows=None):
+                     cu_docs, sinks, mode, scale, rows=None, bufs=None):
     """Block-sparse causal attention with a document mask.
 
     q ``[B*S,Hq,D]``, k/v ``[B*S,Hkv,D]`` (uint16 bf16 bits), block_table
@@ -131,9 +145,9 @@ def block_sparse_fwd(q, k, v, batch, seq_len, block_table, block_size,
     hkv = k.shape[1]
     s = _sinks(sinks, hq)
     b, e = (0, T) if rows is None else rows
-    out = np.full((T, hq, d), np.nan)
-    lse = np.full((hq, T), np.nan)
-    cnt = np.full((T,), -1, np.int32)
+    out, lse, cnt = _outputs(bufs, "block", (((T, hq, d), np.float64, np.nan),
+                                             ((hq, T), np.float64, np.nan),
+                                             ((T,), np.int32, -1)))
     rc = _lib().oracle_block_sparse_fwd(
         _ptr(q), _ptr(k), _ptr(v), int(batch), int(seq_len), hq, hkv, d,
         _ptr(tab), tab.shape[1], int(block_size), _ptr(cd), len(cd) - 1,
@@ -193,7 +207,8 @@ def e4m3_to_f64(codes):
     return s * v
 
 
-def sparse_index_fwd_fp8(q, kv, kv_scale, indices, dv, sinks, mode, scale, rows=None):
+def sparse_index_fwd_fp8(q, kv, kv_scale, indices, dv, sinks, mode, scale, rows=None,
+                         bufs=None):
     """Top-k index attention into an e4m3 latent cache: latent row r is
     ``e4m3(kv[r]) * kv_scale[r]`` (fp64), K the whole row, V its first ``dv``
     columns; otherwise as ``sparse_index_fwd`` (afierka-intel/vllm pull 76,
@@ -206,9 +221,9 @@ def sparse_index_fwd_fp8(q, kv, kv_scale, indices, dv, sinks, mode, scale, rows=
     nkv = kv.shape[0]
     idx = np.asarray(indices, np.int64)
     b, e = (0, nq) if rows is None else rows
-    out = np.full((nq, hq, dv), np.nan)
-    lse = np.full((hq, nq), np.nan)
-    cnt = np.full((nq,), -1, np.int32)
+    out, lse, cnt = _outputs(bufs, "index_fp8", (((nq, hq, dv), np.float64, np.nan),
+                                                 ((hq, nq), np.float64, np.nan),
+                                                 ((nq,), np.int32, -1)))
     sk = np.asarray(sinks, np.float64) if sinks is not None else np.zeros(hq)
     for i in range(b, e):
         keys = idx[i][(idx[i] >= 0) & (idx[i] < nkv)]
@@ -230,7 +245,7 @@ def sparse_index_fwd_fp8(q, kv, kv_scale, indices, dv, sinks, mode, scale, rows=
     return out, lse, cnt
 
 
-def block_select(index_q, index_k, batch, seq_len, block_size, topk, rows=None):
+def block_select(index_q, index_k, batch, seq_len, block_size, topk, rows=None, bufs=None):
     """Top-k key blocks per (index head, query token) from indexer scores
     ([M3 CP sparse] forward step 3 and ``_select_local_blocks``: the selection
     is built from index q / k over the causal sequence of the token's batch
@@ -254,8 +269,8 @@ def block_select(index_q, index_k, batch, seq_len, block_size, topk, rows=None):
     T, hi, di = qf.shape
     nb = -(-seq_len // block_size)
     b0, e0 = (0, T) if rows is None else rows
-    table = np.full((hi, T, topk), -2, np.int32)
-    scores = np.full((hi, T, nb), np.nan)
+    table, scores = _outputs(bufs, "select", (((hi, T, topk), np.int32, -2),
+                                              ((hi, T, nb), np.float64, np.nan)))
     table[:, b0:e0] = -1
     for i in range(b0, e0):
         row0 = (i // seq_len) * seq_len
@@ -279,7 +294,7 @@ def block_select(index_q, index_k, batch, seq_len, block_size, topk, rows=None):
 
 
 def block_sparse_fwd_index_heads(q, k, v, batch, seq_len, tables, block_size, cu_docs,
-                                 sinks, mode, scale, rows=None):
+                                 sinks, mode, scale, rows=None, bufs=None):
     """Block-sparse attention with one selection per index head: attention
     head h uses ``tables[h // (Hq / Hi)]`` ([M3 CP sparse] ``_select_local_blocks``
     returns ``[batch, index_heads, sequence, key_blocks]``); each group of
@@ -296,16 +311,16 @@ def block_sparse_fwd_index_heads(q, k, v, batch, seq_len, tables, block_size, cu
         raise ValueError("the number of index heads must divide the KV heads")
     gq, gk = hq // hi, hkv // hi
     s = _sinks(sinks, hq)
-    out = np.full((T, hq, d), np.nan)
-    lse = np.full((hq, T), np.nan)
-    cnt = np.full((hi, T), -1, np.int32)
+    out, lse, cnt = _outputs(bufs, "block_heads", (((T, hq, d), np.float64, np.nan),
+                                                   ((hq, T), np.float64, np.nan),
+                                                   ((hi, T), np.int32, -1)))
     for g in range(hi):
         o, l, c = block_sparse_fwd(
             np.ascontiguousarray(np.asarray(q)[:, g * gq:(g + 1) * gq]),
             np.ascontiguousarray(np.asarray(k)[:, g * gk:(g + 1) * gk]),
             np.ascontiguousarray(np.asarray(v)[:, g * gk:(g + 1) * gk]),
             batch, seq_len, tables[g], block_size, cu_docs,
-            s[g * gq:(g + 1) * gq], mode, scale, rows=rows)
+            s[g * gq:(g + 1) * gq], mode, scale, rows=rows, bufs=bufs)
         out[:, g * gq:(g + 1) * gq] = o
         lse[g * gq:(g + 1) * gq] = l
         cnt[g] = c

@@ -167,6 +167,41 @@ def test_sparse_index_empty_batch_is_a_no_op(lib):
     assert _index_call(lib, nq=0) == 0
 
 
+def _noalloc_call(lib, **kw):
+    a = dict(q=16, kv=16, nkv=1000, dqk=576, dv=512, idx=16, topk=2048, nq=4,
+             hq=128, sinks=16, mode=2, scale=0.04, out=16, lse=16)
+    a.update(kw)
+    return lib.sa_sparse_index_fwd_noalloc(
+        a["q"], a["kv"], a["nkv"], a["dqk"], a["dv"], a["idx"], a["topk"], a["nq"],
+        a["hq"], a["sinks"], a["mode"], a["scale"], a["out"], a["lse"], None)
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(q=None), 1, "NULL"),
+    (dict(mode=5), 1, "sink_mode"),
+    (dict(sinks=None), 1, "sinks is NULL"),
+    (dict(nkv=0), 1, "bad sizes"),
+    (dict(kv=24), 1, "misaligned"),
+    (dict(mode=1), 2, "KEY0_BIAS"),
+    (dict(nkv=1 << 31), 2, "num_kv"),
+    # argument errors come before the scratch-size check, even for sizes
+    # whose scratch would exceed the fixed array
+    (dict(topk=9000), 2, "topk 9000"),
+    (dict(topk=9000, nq=64), 2, "topk 9000"),
+    (dict(dv=256), 2, "dqk 576 / dv 256"),
+    # 64 queries x 128 heads x 8 items of partials: beyond the fixed 64 MiB
+    (dict(nq=64), 2, "64 MiB"),
+])
+def test_sparse_index_noalloc_rejects_bad_arguments(lib, kw, status, needle):
+    assert _noalloc_call(lib, **kw) == status
+    msg = lib.sa_last_error().decode()
+    assert needle in msg and msg.startswith("sa_sparse_index_fwd_noalloc:"), msg
+
+
+def test_sparse_index_noalloc_empty_batch_is_a_no_op(lib):
+    assert _noalloc_call(lib, nq=0) == 0
+
+
 def _block_call(lib, **kw):
     a = dict(q=16, k=16, v=16, batch=2, S=8192, hq=32, hkv=4, d=128, tab=16, topk=16,
              bs=64, cu=16, ndocs=6, sinks=16, mode=2, scale=0.08, out=16, lse=16)

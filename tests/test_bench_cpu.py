@@ -17,7 +17,7 @@ def test_workload_builds_and_counts(name):
     r = bench.RUNNERS[name](name)
     cfg = r.config()
     assert cfg["workload"] == name
-    assert r.bound in ("hbm", "tensor")
+    assert r.bound in ("hbm", "tensor", "launch")
     assert os.path.exists(os.path.join(ROOT, r.source))
     nbytes, flops = r.counts()
     assert nbytes > 0 and flops > 0

@@ -63,6 +63,35 @@ def test_mla_sparse_decode_per_valid_count():
         assert rel <= REL_L2_TOL and dl <= LSE_TOL, (cnt, rel, dl)
 
 
+def test_full_size_null_sink_is_applied_on_short_rows():
+    """The full decode batch in the benchmark's launch configuration: for the
+    short lists (1, 4 and 16 valid keys) the NULL_LOGIT output must differ
+    from the no-sink output far beyond the tolerance, and the difference must
+    be the oracle's, row by row (a row whose sink were dropped would show a
+    difference of zero)."""
+    from tests.gpu_util import ROW_REL_TOL, row_errors
+    c = W.mla_sparse_decode(NULL)
+    o2, l2 = gpu_run(c, NULL)
+    o0, _ = gpu_run(c, NONE)
+    r2, rl2, n = O.sparse_index_fwd(c.q, c.kv, c.indices, c.dv, c.sinks, NULL, c.scale)
+    r0, _, _ = O.sparse_index_fwd(c.q, c.kv, c.indices, c.dv, c.sinks, NONE, c.scale)
+    g2 = o2.float().cpu().numpy().astype(np.float64)
+    g0 = o0.float().cpu().numpy().astype(np.float64)
+    nr = np.linalg.norm(r2, axis=-1)
+    scale = np.maximum(nr, 0.1 * np.sqrt(np.mean(nr ** 2)))
+    err = np.linalg.norm((g2 - g0) - (r2 - r0), axis=-1) / scale
+    assert err.max() <= 2 * ROW_REL_TOL, (np.unravel_index(err.argmax(), err.shape), err.max())
+    for cnt in (1, 4, 16):
+        rows = np.nonzero(n == cnt)[0]
+        moved = np.linalg.norm((g2 - g0)[rows]) / np.linalg.norm(r2[rows])
+        assert moved >= 30 * REL_L2_TOL, (cnt, moved)  # oracle: 1.14, 0.45, 0.15
+        sig = (np.linalg.norm((r2 - r0)[rows], axis=-1) / scale[rows])
+        assert (sig > 4 * ROW_REL_TOL).mean() >= 0.5
+    assert row_errors(g2, r2).max() <= ROW_REL_TOL
+    rel, dl = compare(o2, l2, r2, rl2)
+    assert rel <= REL_L2_TOL and dl <= LSE_TOL
+
+
 def test_neg_inf_sink_is_bitwise_no_sink():
     import torch
     c = W.mla_sparse_decode(NULL, seed=1204)

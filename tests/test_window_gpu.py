@@ -197,3 +197,48 @@ def test_gqa_window_16k(mode):
     c = W.gqa_window(mode)
     assert min(np.diff(c.cu_seqlens)) < c.window_left
     check(c, mode)
+
+
+def _first_window_rows(c):
+    """Query rows whose key set holds their sequence's first key."""
+    cu = c.cu_seqlens.astype(np.int64)
+    rows = [np.arange(cu[b], min(cu[b + 1], cu[b] + c.window_left + 1))
+            for b in range(len(cu) - 1)]
+    return np.concatenate(rows)
+
+
+@pytest.mark.parametrize("which", ["vision16384", "gqa16384"])
+def test_full_size_key0_sink_is_applied_on_every_first_window_row(which):
+    """On the full vision and GQA blocks, in the benchmark's launch
+    configuration: on the rows that reach their sequence's first key, the
+    KEY0_BIAS output must differ from the no-sink output far beyond the
+    tolerance, and the difference itself must be the oracle's, row by row
+    (a row whose sink were dropped would show a difference of zero)."""
+    from tests.gpu_util import ROW_REL_TOL, row_errors
+    c = W.vision_window(16384, KEY0) if which == "vision16384" else W.gqa_window(KEY0)
+    rows = _first_window_rows(c)
+    o_k0, l_k0 = gpu_run(c, KEY0)
+    o_no, _ = gpu_run(c, NONE)
+    r_k0, rl_k0 = oracle_run(c, KEY0)
+    r_no, _ = oracle_run(c, NONE)
+    g_k0 = o_k0.float().cpu().numpy().astype(np.float64)[rows]
+    g_no = o_no.float().cpu().numpy().astype(np.float64)[rows]
+    ref = r_k0[rows]
+    # whole first-window block: the sink moves it far beyond the tolerance
+    moved = np.linalg.norm(g_k0 - g_no) / np.linalg.norm(ref)
+    assert moved >= 5 * REL_L2_TOL, moved
+    # row by row: the GPU's sink effect equals the oracle's
+    d_gpu, d_ref = g_k0 - g_no, ref - r_no[rows]
+    scale = np.maximum(np.linalg.norm(ref, axis=-1),
+                       0.1 * np.sqrt(np.mean(np.linalg.norm(ref, axis=-1) ** 2)))
+    err = np.linalg.norm(d_gpu - d_ref, axis=-1) / scale
+    assert err.max() <= 2 * ROW_REL_TOL, (np.unravel_index(err.argmax(), err.shape), err.max())
+    # the check has teeth: on at least a tenth of the (row, head) pairs the
+    # sink moves the row by more than twice the bound above (vision block:
+    # 14 %, GQA block: 59 %), so a dropped sink there fails it
+    sig = np.linalg.norm(d_ref, axis=-1) / scale
+    assert (sig > 4 * ROW_REL_TOL).mean() >= 0.1
+    # and the KEY0 rows themselves are within the per-row parity bound
+    assert row_errors(g_k0, ref).max() <= ROW_REL_TOL
+    rel, dl = compare(o_k0, l_k0, r_k0, rl_k0)
+    assert rel <= REL_L2_TOL and dl <= LSE_TOL
