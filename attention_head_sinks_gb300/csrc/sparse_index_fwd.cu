@@ -10,41 +10,35 @@
 // Layout: the latent row holds 576 values (512 latent + 64 rope); K is the
 // whole row and V its first 512 values, shared by all query heads.
 //
-// Three kernels, back to back on the stream (the second and third start
-// early under programmatic dependent launch and wait for their input):
+// Two kernels, back to back on the stream (the second starts early under
+// programmatic dependent launch and waits for the first):
 //  1. plan: one CTA per query compacts the valid entries of its index row
-//     (order kept) into the workspace and stores their count c.  A query with
-//     c = 0 gets its zero output and LSE = -inf here.
-//  2. attend: the compacted list of a query is cut into items of up to 256
-//     keys; CTA b takes item b of the order "all full 256-key items (query
-//     order), then the shorter last items (query order)", so the long items
-//     start first and the CTAs past the last item leave at once.  One CTA
-//     per (item, block of 128 heads):
+//     (order kept) into the workspace, stores their count c and clears the
+//     query's completion counter.  A query with c = 0 gets its zero output and
+//     LSE = -inf here.
+//  2. attend, persistent (one CTA per SM at most): the compacted list of a
+//     query is cut into items of up to 256 keys, ordered "all full 256-key
+//     items (query order), then the shorter last items (query order)", and
+//     CTA b takes items b, b + grid, ... (so the long items start first and
+//     no CTA is launched without work).  Per (item, block of 128 heads):
 //       S = Q K^T      M = 128 heads, N = item keys (rounded to 16), K = 576
 //                      in nine 64-wide slabs;
 //       O_half = P V   twice, N = 256 V columns each, K = the item's keys.
-//  3. combine: queries with more than one item merge the (O, m, l) partials
-//     and fold the sink once.
-// A query with a single item is finished by its attend CTA (sink fold, bf16
-// O, LSE).
-//
-// Attend CTA.  Tensor memory: S at columns [0, 256) (P in place, bf16, the A
-// operand of P V), O_half at [256, 512).  Shared memory: six 32 KB slots
-// R0 R1 R2 R3 K0 K1 of gathered 64-column slabs, 128-byte swizzled (the
-// K-major B operand of S, the MN-major B operand of P V), and two 16 KB Q
-// slab buffers fed by TMA.  Slabs 0..3 (V columns 0..255) sit in R0..R3;
-// slabs 8, 4, 5, 7, 6 stream through K0/K1, so that after S the ring holds
-// K0 = slab 6, K1 = slab 7.  After the first P V, slabs 4 and 5 are gathered
-// again (from L2) into R2, R3 and the second P V reads R2 R3 K0 K1 = slabs
-// 4..7.  Warps 4..7 gather rows with 16-byte cp.async copies; thread 0
-// issues the MMAs, thread 32 the Q loads; all eight warps then share the
-// softmax and the epilogues (warps w and w + 4 split the columns of the same
-// 32 TMEM lanes).
+//     A query with a single item is finished there (sink fold, bf16 O, LSE).
+//     Otherwise the item's (O, m, l) partial goes to the workspace and the
+//     query's completion counter is raised.  Once a CTA has no items left it
+//     merges: units of (query with several items, block of 128 heads, 16 V
+//     columns) are dealt round-robin over the CTAs; a unit waits (bounded)
+//     for its query's counter, then merges the partials by their LSE weights
+//     and folds the sink once.  Every CTA of the grid is resident (one per
+//     SM), and a CTA merges only after finishing its own items, so every
+//     wait ends.
 // Split-KV partials are stored heads-fastest ([query][item][column][head],
 // the head stride rounded up to 32), so each warp store of the epilogue
 // writes 128 contiguous, aligned bytes.
 #include <cuda_bf16.h>
 #include <math.h>
+#include <string.h>
 
 #include <algorithm>
 #include <mutex>
@@ -71,6 +65,19 @@ constexpr int kColS = 0;
 constexpr int kColO = 256;
 constexpr int kMaxSlices = 32;  // topk <= 32 * 256
 constexpr int kThreads = 256;
+constexpr int kMergeCols = 16;  // V columns per merge unit
+constexpr int kMergeGroup = 8;  // items whose partials are loaded at once
+constexpr int kMergeStages = 3; // merge units in flight per CTA (TMA-fed)
+
+// One merge unit's partials in shared memory: the [8 items][16 columns][128
+// heads] O box and the [8 items x (m, l)][128 heads] box, fp32, row stride the
+// tile's head count.
+struct __align__(128) MergeStage {
+  float o[kMergeGroup][kMergeCols][128];
+  float ml[kMergeGroup][2][128];
+};
+static_assert(kMergeStages * sizeof(MergeStage) <= kNumSlots * kSlotBytes + 2 * kSlabBytesQ,
+              "merge stages reuse the attend buffers");
 
 // S step j: slab of Q/K and the slot it sits in (0..3 = R0..R3, 4 = K0,
 // 5 = K1).  The ring slabs come first so that the ring refills overlap the
@@ -92,6 +99,7 @@ struct PlanParams {
   int32_t num_q_heads;
   int32_t* cidx;    // [nq, topk]: valid entries first, in order
   int32_t* qcount;  // [nq]
+  int32_t* done;    // [nq]: items (x head blocks) finished, cleared here
   __nv_bfloat16* out;
   float* lse;
 };
@@ -112,7 +120,7 @@ struct IndexParams {
   float* part_o;          // [nq][nslices][512][head_stride]
   float* part_ml;         // [nq][nslices][2][head_stride]  (m, then l)
   int32_t head_stride;    // num_q_heads rounded up to 32
-  int32_t combine_min_items;  // the warp-unit combine takes queries with at least this many items
+  int32_t* done;          // [nq]: items x head blocks finished (merge readiness)
   uint32_t* err;
 };
 
@@ -124,9 +132,13 @@ struct __align__(8) IndexSmemCtl {
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_full;
-  uint64_t o_full;           // phase 0: first V half, phase 1: second
+  uint64_t oa_full;          // O of V columns 0..255 (slabs 0..3)
+  uint64_t ob1_full;         // O of V columns 384..511 (slabs 6, 7)
+  uint64_t ob2_full;         // O of V columns 256..383 (slabs 4, 5, gathered again)
   uint32_t tmem_base;
   int32_t item_q, item_s, item_n, item_nitems;
+  int32_t merge_ok;
+  uint64_t merge_full[kMergeStages];
   int32_t scan_f[8], scan_p[8];
   int32_t kidx[kItemKeys];  // the item's key rows
 };
@@ -176,6 +188,11 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
@@ -216,6 +233,7 @@ __device__ __forceinline__ int block_exclusive_sum(int x, int* scratch, int* tot
 __global__ void __launch_bounds__(kThreads)
 sparse_index_plan_kernel(const PlanParams p) {
   griddep_launch_dependents();
+  griddep_wait();  // the previous call's kernels may still read the workspace
   __shared__ int32_t s_cnt[kMaxSlices * 8];
   __shared__ int32_t s_pre[kMaxSlices * 8];
   __shared__ int32_t s_scan[8];
@@ -248,7 +266,10 @@ sparse_index_plan_kernel(const PlanParams p) {
     const uint32_t bal = __ballot_sync(0xffffffffu, ok);
     if (ok) crow[s_pre[c * 8 + warp] + __popc(bal & lt)] = v[c];
   }
-  if (tid == 0 && p.qcount) p.qcount[q] = total;
+  if (tid == 0 && p.qcount) {
+    p.qcount[q] = total;
+    p.done[q] = 0;
+  }
   if (total == 0) {
     // empty key set: zero output, LSE = -inf
     uint4* dst = reinterpret_cast<uint4*>(p.out + (int64_t)q * p.num_q_heads * kDv);
@@ -260,35 +281,46 @@ sparse_index_plan_kernel(const PlanParams p) {
 // ---------------------------------------------------------------------------
 // 2. attend
 
-// Item `item` of the global order (see the file header) -> ctl.item_*; q = -1
-// past the last item.  All 256 threads take part.  Thread t owns queries
-// [t K, t K + K), K = ceil(nq / 256).
-__device__ void find_item(const IndexParams& p, int item, IndexSmemCtl& ctl) {
+// The global item order (see the file header).  scan_items() takes the
+// prefix sums once (all 256 threads; thread t owns queries [t K, t K + K),
+// K = ceil(nq / 256)); lookup_item() then resolves item `item` into
+// ctl.item_* (q = -1 past the last item).  Both contain __syncthreads.
+struct ItemScan {
+  int pre_f, pre_p, nfull, npart, tot_f, tot_p;
+};
+
+__device__ ItemScan scan_items(const IndexParams& p, IndexSmemCtl& ctl) {
   const int tid = threadIdx.x;
   const int K = (p.nq + kThreads - 1) / kThreads;
-  const int q0 = tid * K;
-  int cache[4];
-  int nfull = 0, npart = 0;
+  ItemScan sc;
+  sc.nfull = 0;
+  sc.npart = 0;
   for (int i = 0; i < K; ++i) {
-    const int qq = q0 + i;
+    const int qq = tid * K + i;
     const int c = qq < p.nq ? __ldcg(p.qcount + qq) : 0;
-    if (i < 4) cache[i & 3] = c;
-    nfull += c / kItemKeys;
-    npart += (c % kItemKeys) != 0 ? 1 : 0;
+    sc.nfull += c / kItemKeys;
+    sc.npart += (c % kItemKeys) != 0 ? 1 : 0;
   }
+  sc.pre_f = block_exclusive_sum(sc.nfull, ctl.scan_f, &sc.tot_f);
+  sc.pre_p = block_exclusive_sum(sc.npart, ctl.scan_p, &sc.tot_p);
+  return sc;
+}
+
+__device__ void lookup_item(const IndexParams& p, const ItemScan& sc, int item,
+                            IndexSmemCtl& ctl) {
+  const int tid = threadIdx.x;
+  const int K = (p.nq + kThreads - 1) / kThreads;
   if (tid == 0) ctl.item_q = -1;
-  int tot_f = 0, tot_p = 0;
-  const int pre_f = block_exclusive_sum(nfull, ctl.scan_f, &tot_f);
-  const int pre_p = block_exclusive_sum(npart, ctl.scan_p, &tot_p);
-  const bool heavy = item < tot_f;
-  const int target = heavy ? item : item - tot_f;
-  const int pre = heavy ? pre_f : pre_p;
-  const int mine = heavy ? nfull : npart;
-  if ((heavy || target < tot_p) && pre <= target && target < pre + mine) {
+  __syncthreads();
+  const bool heavy = item < sc.tot_f;
+  const int target = heavy ? item : item - sc.tot_f;
+  const int pre = heavy ? sc.pre_f : sc.pre_p;
+  const int mine = heavy ? sc.nfull : sc.npart;
+  if ((heavy || target < sc.tot_p) && pre <= target && target < pre + mine) {
     int acc = pre;
     for (int i = 0; i < K; ++i) {
-      const int qq = q0 + i;
-      const int c = i < 4 ? cache[i & 3] : __ldcg(p.qcount + qq);
+      const int qq = tid * K + i;
+      const int c = __ldcg(p.qcount + qq);
       const int f = c / kItemKeys, r = c % kItemKeys;
       const int here = heavy ? f : (r != 0 ? 1 : 0);
       if (target < acc + here) {
@@ -395,7 +427,10 @@ __device__ __forceinline__ void gather_slab(uint32_t dst, const uint16_t* kv,
 
 template <int MODE, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv_raw,
+sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_part,
+                        const __grid_constant__ CUtensorMap tm_part1,
+                        const __grid_constant__ CUtensorMap tm_ml, const void* kv_raw,
                         const IndexParams p) {
   // bf16 cache: rows of 576 bf16; fp8 cache: rows of 576 e4m3 bytes
   const uint16_t* kv = reinterpret_cast<const uint16_t*>(kv_raw);
@@ -412,8 +447,24 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   griddep_launch_dependents();
+  if (warp == 0) {
+    tmem_alloc(&ctl.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  griddep_wait();  // the plan kernel's counts and lists are complete
+  const ItemScan isc = scan_items(p, ctl);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  // work w = (item w / nhb, head block w % nhb); CTA b takes w = b, b + grid, ...
+  const int nwork = (isc.tot_f + isc.tot_p) * p.nhb;
 
+  for (int w = (int)blockIdx.x; w < nwork; w += (int)gridDim.x) {
+  lookup_item(p, isc, w / p.nhb, ctl);
   if (tid == 0) {
+    // every barrier starts each item at phase 0 (the previous item's
+    // arrivals have all landed: its last waits saw them)
     for (int i = 0; i < 4; ++i) mbar_init(&ctl.res_full[i], 128);
     mbar_init(&ctl.res2_full, 128);
     for (int s2 = 0; s2 < 2; ++s2) {
@@ -423,23 +474,16 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
       mbar_init(&ctl.q_empty[s2], 1);
     }
     mbar_init(&ctl.s_full, 1);
-    mbar_init(&ctl.o_full, 1);
+    mbar_init(&ctl.oa_full, 1);
+    mbar_init(&ctl.ob1_full, 1);
+    mbar_init(&ctl.ob2_full, 1);
     fence_mbar_init();
   }
-  if (warp == 0) {
-    tmem_alloc(&ctl.tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  griddep_wait();  // the plan kernel's counts and lists are complete
-  find_item(p, (int)(blockIdx.x / p.nhb), ctl);
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = ctl.tmem_base;
   const int q = ctl.item_q;
 
   if (q >= 0) {
-    const int hb = blockIdx.x % p.nhb;
+    const int hb = w % p.nhb;
     const int slice = ctl.item_s;
     const int n = ctl.item_n;
     const bool direct = ctl.item_nitems == 1;  // this CTA writes the final output
@@ -574,9 +618,13 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
         tma_load_2d(s_qst + st * kSlabBytesQ, &tm_q, &ctl.q_full[st], step_slab(j) * kSlab, qrow0);
         ++issued;
       }
-      // bounded drain of the last copies (immediate once the MMAs consumed them)
-      for (int j = max(0, issued - 2); j < issued; ++j)
+      // bounded drain of the last copies (immediate once the MMAs consumed
+      // them), and of the MMAs' releases of them: no arrival may follow the
+      // next item's barrier initialisation
+      for (int j = max(0, issued - 2); j < issued; ++j) {
         mbar_wait(&ctl.q_full[j & 1], (j >> 1) & 1, p.err, kErrWaitDrain);
+        mbar_wait(&ctl.q_empty[j & 1], (j >> 1) & 1, p.err, kErrWaitDrain);
+      }
     }
 
     // ---- softmax: thread (row, part) takes key columns [128 part, +128) ----
@@ -710,34 +758,52 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
       inv = alpha / den;
     }
 
-    // ---- O_half = P V_half (thread 0), then the epilogue of that half ------
-    auto issue_pv = [&](int first_slot) {
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, 256, true);
+    // ---- O = P V in three parts (thread 0 issues), each with its epilogue ----
+    // After S the resident slabs are 0..3 (R0..R3) and 6, 7 (K0, K1):
+    //   A:  V columns 0..255   <- R0..R3, N = 256, into TMEM [256, 512);
+    //   B1: V columns 384..511 <- K0, K1, N = 64 each, into the S columns
+    //       the softmax left free, [64, 128) and [192, 256) (P sits in
+    //       [0, 64) and [128, 192));
+    //   B2: V columns 256..383 <- slabs 4, 5 gathered again over R2, R3 once
+    //       A has read them, N = 128, into TMEM [256, 384) once the
+    //       epilogue of A has read it.
+    // A and B1 go to the tensor pipe together; the regather overlaps the
+    // epilogue of A, and B2 the epilogue of B1.
+    auto issue_pv = [&](int first_slot, uint32_t col, int ncols) {
+      const uint32_t idesc = idesc_bf16(128, ncols, true);
       const uint32_t vb = slot_u32(first_slot);
       for (int kk = 0; kk < npad / 16; ++kk) {
         // P of keys [16 kk, 16 kk + 16): TMEM column 8 kk (keys < 128) or
         // 128 + 8 (kk - 8)
         const uint32_t pa = tmem + kColS + (kk < 8 ? kk * 8 : 128 + (kk - 8) * 8);
         const uint64_t b = smem_desc(vb + kk * 16 * 128, kSlotBytes, 1024, kLayoutSw128);
-        mma_ts(tmem + kColO, pa, b, idesc, kk > 0 ? 1u : 0u);
+        mma_ts(tmem + col, pa, b, idesc, kk > 0 ? 1u : 0u);
       }
-      mma_commit(&ctl.o_full);
     };
     if (tid == 0) {
-      if (ok) issue_pv(0);
-      else mbar_arrive(&ctl.o_full);
+      if (ok) {
+        tc_fence_after();
+        issue_pv(0, kColO, 256);
+        mma_commit(&ctl.oa_full);
+        issue_pv(4, kColS + 64, 64);
+        issue_pv(5, kColS + 192, 64);
+        mma_commit(&ctl.ob1_full);
+      } else {
+        mbar_arrive(&ctl.oa_full);
+        mbar_arrive(&ctl.ob1_full);
+      }
     }
     const int64_t hq = p.num_q_heads;
-    auto epilogue = [&](int half) {
-      const int col0 = half * 256 + part * 128;  // V column of this thread's first value
-      __nv_bfloat16* orow = p.out + ((int64_t)q * hq + h) * kDv + col0;
+    // this thread's row, nch chunks of 32 values: TMEM columns tcol + 32 j,
+    // V columns vcol + 32 j
+    auto epilogue = [&](int tcol, int vcol, int nch) {
+      __nv_bfloat16* orow = p.out + ((int64_t)q * hq + h) * kDv + vcol;
       const int64_t hs = p.head_stride;
-      float* pcol = p.part_o + (((int64_t)q * p.nslices + slice) * kDv + col0) * hs + h;
+      float* pcol = p.part_o + (((int64_t)q * p.nslices + slice) * kDv + vcol) * hs + h;
 #pragma unroll 1
-      for (int jj = 0; jj < 4; ++jj) {
+      for (int jj = 0; jj < nch; ++jj) {
         float o[32];
-        tmem_ld32(lane_base + kColO + part * 128 + 32 * jj, o);
+        tmem_ld32(lane_base + tcol + 32 * jj, o);
         tmem_wait_ld();
         if (row_valid && direct) {
 #pragma unroll
@@ -755,12 +821,11 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
         }
       }
     };
-    ok = mbar_wait(&ctl.o_full, 0, p.err, kErrWaitMma) && ok;
+    ok = mbar_wait(&ctl.oa_full, 0, p.err, kErrWaitMma) && ok;
     __syncwarp();
     tc_fence_after();
     if (warp >= 4) {
-      // slabs 4, 5 over R2, R3 (the first P V has read them), landing while
-      // the first half is stored
+      // slabs 4, 5 over R2, R3 (A has read them), landing while A is stored
       if (ok) {
         if (FP8) {
           stage_slab_fp8(slot_u32(2), kv8, ctl.kidx, npad, n, fr0, fc4, 4);
@@ -771,7 +836,7 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
         }
       }
       cp_async_commit();
-      epilogue(0);
+      epilogue(kColO + part * 128, part * 128, 4);
       cp_async_wait<0>();
       if (FP8) {
         convert_slab_fp8(slot_u32(2), npad, fr0, fc4);
@@ -780,19 +845,27 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
       fence_proxy_async();
       mbar_arrive(&ctl.res2_full);
     } else {
-      epilogue(0);
+      epilogue(kColO + part * 128, part * 128, 4);
     }
     tc_fence_before();
-    __syncthreads();  // every TMEM read of the first half is done
+    __syncthreads();  // every TMEM read of A is done
     if (tid == 0) {
       tc_fence_after();
-      if (ok && mbar_wait(&ctl.res2_full, 0, p.err, kErrWaitLoad)) issue_pv(2);
-      else mbar_arrive(&ctl.o_full);
+      if (ok && mbar_wait(&ctl.res2_full, 0, p.err, kErrWaitLoad)) {
+        issue_pv(2, kColO, 128);
+        mma_commit(&ctl.ob2_full);
+      } else {
+        mbar_arrive(&ctl.ob2_full);
+      }
     }
-    ok = mbar_wait(&ctl.o_full, 1, p.err, kErrWaitMma) && ok;
+    ok = mbar_wait(&ctl.ob1_full, 0, p.err, kErrWaitMma) && ok;
     __syncwarp();
     tc_fence_after();
-    epilogue(1);
+    epilogue(kColS + 64 + part * 128, 384 + part * 64, 2);
+    ok = mbar_wait(&ctl.ob2_full, 0, p.err, kErrWaitMma) && ok;
+    __syncwarp();
+    tc_fence_after();
+    epilogue(kColO + part * 64, 256 + part * 64, 2);
     if (row_valid && part == 0) {
       if (direct) {
         p.lse[(int64_t)h * p.nq + q] = (m + log2f(l)) * kLn2;
@@ -800,6 +873,215 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
         float* ml = p.part_ml + ((int64_t)q * p.nslices + slice) * 2 * p.head_stride + h;
         ml[0] = m;
         ml[p.head_stride] = l;
+      }
+    }
+    if (!direct) {
+      // this item's partial is written: count it for the query's merge
+      __syncthreads();
+      if (tid == 0) {
+        __threadfence();
+        atomicAdd(p.done + q, 1);
+      }
+    }
+  }
+  // the next item rewrites tensor memory and the barriers
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  }  // items
+
+  // ---- split-KV merge -------------------------------------------------------------
+  // Units of (query with several items, block of 128 heads, 16 V columns),
+  // dealt round-robin over the CTAs, 256 queries at a time; a unit waits
+  // (bounded) until every item of its query is counted.  Thread t merges
+  // head t mod 128 of the unit's head block, V columns 8 (t / 128) .. + 8:
+  //   O = sum_s 2^(m_s - M) O_s * alpha / (L alpha + 2^(s_h log2e - M')),
+  //   M = max m_s, L = sum_s l_s 2^(m_s - M), M' = max(M, s_h log2e),
+  //   alpha = 2^(M - M'), LSE = (M + log2 L) ln 2 over the listed keys only.
+  // Queries of at most eight items: thread 0 loads each unit with two TMA
+  // copies into one of three shared-memory stages (the attend buffers, free
+  // now), so three units' reads are in flight without register cost.  More
+  // items: plain loads, eight items at a time.
+  {
+    const int h_in = tid & 127, half = tid >> 7;
+    const int64_t hs = p.head_stride;
+    const int bi = hs < 128 ? (int)hs : 128;  // heads per TMA box row
+    constexpr int kUnitsPerHb = kDv / kMergeCols;
+    const int64_t per_q = (int64_t)p.nhb * kUnitsPerHb;
+    const int64_t G = gridDim.x;
+    MergeStage* stage = reinterpret_cast<MergeStage*>(s_slot);
+    // the stages overlay buffers this CTA wrote through the generic proxy
+    // (the softmax exchange); order those writes before the copies' writes
+    fence_proxy_async();
+    if (tid == 0) {
+      for (int i = 0; i < kMergeStages; ++i) mbar_init(&ctl.merge_full[i], 1);
+      fence_mbar_init();
+      tma_prefetch_map(&tm_part);
+      tma_prefetch_map(&tm_part1);
+      tma_prefetch_map(&tm_ml);
+      ctl.merge_ok = 1;
+    }
+    __syncthreads();
+    // thread 0: wait (bounded) until query q's items are all counted
+    auto wait_ready = [&](int q, int ns) -> bool {
+      const int want = ns * p.nhb;
+      if (ld_acquire(p.done + q) >= want) return true;
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire(p.done + q) < want) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(p.err, kErrWaitLoad);
+          return false;
+        }
+        __nanosleep(64);
+      }
+      return true;
+    };
+    // the merged row segment of head h, columns c0 .. c0 + 8, and its LSE
+    auto finish = [&](int q, int h, int c0, float M, float L, const float (&acc)[8]) {
+      float den = L, alpha = 1.f;
+      if (MODE == SA_SINK_NULL_LOGIT) {
+        const float sink2 = __ldg(p.sinks + h) * kLog2e;
+        const float mp = fmaxf(M, sink2);
+        alpha = ex2_approx(M - mp);
+        den = L * alpha + ex2_approx(sink2 - mp);
+      }
+      const float inv = alpha / den;
+      uint4 pk;
+      pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+      pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+      *reinterpret_cast<uint4*>(p.out + ((int64_t)q * p.num_q_heads + h) * kDv + c0) = pk;
+      if (c0 == 0) p.lse[(int64_t)h * p.nq + q] = (M + log2f(L)) * kLn2;
+    };
+    uint32_t phase = 0;
+    // pass 0: queries of 2..8 items (TMA-fed); pass 1: more than 8 (plain loads)
+    for (int pass = 0; pass < 2; ++pass) {
+      int64_t ubase = 0;
+      for (int qc = 0; qc < p.nq; qc += kThreads) {
+        const int qq = qc + tid;
+        const int nsq = qq < p.nq ? (__ldcg(p.qcount + qq) + kItemKeys - 1) / kItemKeys : 0;
+        const int act = (pass == 0 ? (nsq >= 2 && nsq <= kMergeGroup) : nsq > kMergeGroup) ? 1 : 0;
+        int nact = 0;
+        const int pos = block_exclusive_sum(act, ctl.scan_f, &nact);
+        if (act) ctl.kidx[pos] = qq;
+        __syncthreads();
+        const int64_t nunits = (int64_t)nact * per_q;
+        int64_t first = ((int64_t)blockIdx.x - ubase) % G;
+        if (first < 0) first += G;
+        const int64_t mine = first < nunits ? (nunits - first + G - 1) / G : 0;
+        auto unit_of = [&](int64_t k, int& q, int& hb, int& cb) {
+          const int64_t u = first + k * G;
+          q = ctl.kidx[(int)(u / per_q)];
+          const int r = (int)(u % per_q);
+          hb = r / kUnitsPerHb;
+          cb = r % kUnitsPerHb;
+        };
+        if (pass == 0) {
+          // thread 0: unit k's two copies into stage st, once its query is ready
+          auto issue = [&](int64_t k, int st) {
+            int q, hb, cb;
+            unit_of(k, q, hb, cb);
+            const int ns = (__ldcg(p.qcount + q) + kItemKeys - 1) / kItemKeys;
+            if (!wait_ready(q, ns)) ctl.merge_ok = 0;
+            // the partials were written through the generic proxy by other SMs
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            // full boxes (out-of-range parts zero-filled) count in the
+            // transaction; up to four items one box each, more in one box
+            const int nbox = ns <= 4 ? ns : kMergeGroup;
+            mbar_arrive_expect_tx(&ctl.merge_full[st],
+                                  (uint32_t)((nbox * kMergeCols + 2 * kMergeGroup) * bi * 4));
+            if (ns <= 4) {
+              for (int s2 = 0; s2 < ns; ++s2)
+                tma_load_3d(&stage[st].o[0][0][0] + s2 * kMergeCols * bi, &tm_part1,
+                            &ctl.merge_full[st], hb * 128, cb * kMergeCols, q * p.nslices + s2);
+            } else {
+              tma_load_3d(&stage[st].o[0][0][0], &tm_part, &ctl.merge_full[st], hb * 128,
+                          cb * kMergeCols, q * p.nslices);
+            }
+            tma_load_2d(&stage[st].ml[0][0][0], &tm_ml, &ctl.merge_full[st], hb * 128,
+                        q * p.nslices * 2);
+          };
+          if (tid == 0)
+            for (int64_t k = 0; k < mine && k < kMergeStages; ++k) issue(k, (int)k);
+          for (int64_t k = 0; k < mine; ++k) {
+            const int st = (int)(k % kMergeStages);
+            int q, hb, cb;
+            unit_of(k, q, hb, cb);
+            const int ns = (__ldcg(p.qcount + q) + kItemKeys - 1) / kItemKeys;
+            if (!mbar_wait(&ctl.merge_full[st], (phase >> st) & 1u, p.err, kErrWaitLoad))
+              ctl.merge_ok = 0;
+            phase ^= 1u << st;
+            const int h = hb * 128 + h_in;
+            if (ctl.merge_ok && h < p.num_q_heads) {
+              // box rows: item s has m at row 2 s and l at row 2 s + 1
+              const float* mlt = &stage[st].ml[0][0][0];
+              const float* ot = &stage[st].o[0][0][0];
+              float M = -INFINITY;
+#pragma unroll
+              for (int s2 = 0; s2 < kMergeGroup; ++s2)
+                if (s2 < ns) M = fmaxf(M, mlt[(2 * s2) * bi + h_in]);
+              float L = 0.f, acc[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+              for (int s2 = 0; s2 < kMergeGroup; ++s2) {
+                if (s2 < ns) {
+                  const float wk = ex2_approx(mlt[(2 * s2) * bi + h_in] - M);
+                  L = fmaf(mlt[(2 * s2 + 1) * bi + h_in], wk, L);
+#pragma unroll
+                  for (int e = 0; e < 8; ++e)
+                    acc[e] = fmaf(wk, ot[(s2 * kMergeCols + half * 8 + e) * bi + h_in], acc[e]);
+                }
+              }
+              finish(q, h, cb * kMergeCols + half * 8, M, L, acc);
+            }
+            __syncthreads();  // stage st is consumed
+            if (tid == 0 && k + kMergeStages < mine) issue(k + kMergeStages, st);
+          }
+        } else {
+          for (int64_t k = 0; k < mine; ++k) {
+            int q, hb, cb;
+            unit_of(k, q, hb, cb);
+            const int ns = (__ldcg(p.qcount + q) + kItemKeys - 1) / kItemKeys;
+            if (tid == 0 && !wait_ready(q, ns)) ctl.merge_ok = 0;
+            __syncthreads();
+            const int h = hb * 128 + h_in;
+            if (ctl.merge_ok && h < p.num_q_heads) {
+              const float* ml = p.part_ml + (int64_t)q * p.nslices * 2 * hs + h;
+              const float* po = p.part_o +
+                                ((int64_t)q * p.nslices * kDv + cb * kMergeCols + half * 8) * hs + h;
+              // every item has at least one key, so every l > 0
+              float M = -INFINITY, L = 0.f, acc[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+              for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(ml + s2 * 2 * hs));
+              for (int s0 = 0; s0 < ns; s0 += kMergeGroup) {
+                float wv[kMergeGroup], ov[kMergeGroup][8];
+#pragma unroll
+                for (int k2 = 0; k2 < kMergeGroup; ++k2) {
+                  const bool live = s0 + k2 < ns;
+                  const int64_t si = s0 + k2;
+                  const float mk = live ? __ldcg(ml + si * 2 * hs) : -INFINITY;
+                  const float lk = live ? __ldcg(ml + si * 2 * hs + hs) : 0.f;
+                  wv[k2] = ex2_approx(mk - M);  // 0 for absent items
+                  L = fmaf(lk, wv[k2], L);
+#pragma unroll
+                  for (int e = 0; e < 8; ++e)
+                    ov[k2][e] = live ? __ldcg(po + (si * kDv + e) * hs) : 0.f;
+                }
+#pragma unroll
+                for (int k2 = 0; k2 < kMergeGroup; ++k2)
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) acc[e] = fmaf(wv[k2], ov[k2][e], acc[e]);
+              }
+              finish(q, h, cb * kMergeCols + half * 8, M, L, acc);
+            }
+            __syncthreads();  // ctl.merge_ok may be rewritten by the next unit
+          }
+        }
+        ubase += nunits;
+        __syncthreads();  // ctl.kidx is rewritten by the next chunk
       }
     }
   }
@@ -813,319 +1095,8 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const void* kv
   }
 }
 
-// ---------------------------------------------------------------------------
-// 3a. combine of queries with 2..8 items, TMA-fed.  Units of (query, 16 V
-// columns, 128 heads) are dealt round-robin to one CTA per SM; a CTA keeps
-// three units in flight.  Thread 0 loads a unit with two TMA copies on its
-// mbarrier: the [8 items][16 columns][128 heads] fp32 O box of a 3-D view of
-// the partials and the [8 items x (m, l)][128 heads] box of a 2-D view of
-// the (m, l) rows (items past the query's last are loaded and ignored), so a
-// CTA has ~200 KB of reads outstanding without holding any of it in
-// registers and without paying one copy instruction per item.  Thread t then
-// merges head t mod 128, columns 8 (t / 128) .. + 8 from shared memory (the
-// formula of the warp-unit combine below).
-constexpr int kFcCols = 16;
-constexpr int kFcMaxItems = 8;
-constexpr int kFcStages = 3;
-constexpr int kFcList = 1024;  // queries listed per round
-
-struct __align__(128) FcStage {
-  float o[kFcMaxItems][kFcCols][128];  // row stride: the tile's head count
-  float ml[kFcMaxItems][2][128];
-};
-
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-sparse_index_combine_tma_kernel(const __grid_constant__ CUtensorMap tm_part,
-                                const __grid_constant__ CUtensorMap tm_part1,
-                                const __grid_constant__ CUtensorMap tm_ml, const IndexParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full[kFcStages];
-  __shared__ int32_t s_q[kFcList];
-  __shared__ int32_t s_ns[kFcList];
-  __shared__ int32_t s_scan[8];
-  __shared__ int32_t s_ok;
-  FcStage* stage = reinterpret_cast<FcStage*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    for (int i = 0; i < kFcStages; ++i) mbar_init(&full[i], 1);
-    fence_mbar_init();
-    s_ok = 1;
-    tma_prefetch_map(&tm_part);
-    tma_prefetch_map(&tm_part1);
-    tma_prefetch_map(&tm_ml);
-  }
-  __syncthreads();
-  griddep_wait();  // the attend kernel's partials are complete
-  const int64_t hs = p.head_stride;
-  const int bi = hs < 128 ? (int)hs : 128;  // heads per tile row
-  const int units_per_q = (kDv / kFcCols) * p.nhb;
-  const int64_t G = gridDim.x;
-  const int h = tid & 127, half = tid >> 7;
-  uint32_t phase = 0;
-  int64_t unit_base = 0;
-  for (int qb = 0; qb < p.nq; qb += kFcList) {
-    int nact = 0;
-    for (int r = 0; r < kFcList; r += kThreads) {
-      const int qq = qb + r + tid;
-      const int c = qq < p.nq ? __ldcg(p.qcount + qq) : 0;
-      const int ns = (c + kItemKeys - 1) / kItemKeys;
-      const int act = ns >= 2 && ns <= kFcMaxItems ? 1 : 0;
-      int tot = 0;
-      const int pos = block_exclusive_sum(act, s_scan, &tot);
-      if (act) {
-        s_q[nact + pos] = qq;
-        s_ns[nact + pos] = ns;
-      }
-      nact += tot;
-    }
-    __syncthreads();
-    const int64_t nunits = (int64_t)nact * units_per_q;
-    int64_t first = ((int64_t)blockIdx.x - unit_base) % G;
-    if (first < 0) first += G;
-    const int64_t mine = first < nunits ? (nunits - first + G - 1) / G : 0;
-    auto unit_of = [&](int64_t k, int& q, int& ns, int& colblk, int& hb) {
-      const int64_t u = first + k * G;
-      const int a = (int)(u / units_per_q);
-      const int r = (int)(u % units_per_q);
-      q = s_q[a];
-      ns = s_ns[a];
-      colblk = r % (kDv / kFcCols);
-      hb = r / (kDv / kFcCols);
-    };
-    auto issue = [&](int64_t k, int st) {
-      int q, ns, colblk, hb;
-      unit_of(k, q, ns, colblk, hb);
-      // full boxes (out-of-range parts zero-filled) count in the transaction;
-      // up to four items one box each, more in one eight-item box
-      const int nbox = ns <= 4 ? ns : kFcMaxItems;
-      mbar_arrive_expect_tx(&full[st], (uint32_t)((nbox * kFcCols + 2 * kFcMaxItems) * bi * 4));
-      if (ns <= 4) {
-        for (int s = 0; s < ns; ++s)
-          tma_load_3d(&stage[st].o[0][0][0] + s * kFcCols * bi, &tm_part1, &full[st], hb * 128,
-                      colblk * kFcCols, q * p.nslices + s);
-      } else {
-        tma_load_3d(&stage[st].o[0][0][0], &tm_part, &full[st], hb * 128, colblk * kFcCols,
-                    q * p.nslices);
-      }
-      tma_load_2d(&stage[st].ml[0][0][0], &tm_ml, &full[st], hb * 128, q * p.nslices * 2);
-    };
-    if (tid == 0)
-      for (int64_t k = 0; k < mine && k < kFcStages; ++k) issue(k, (int)k);
-    for (int64_t k = 0; k < mine; ++k) {
-      if (!s_ok) break;  // a load never arrived (error recorded): stop
-      const int st = (int)(k % kFcStages);
-      int q, ns, colblk, hb;
-      unit_of(k, q, ns, colblk, hb);
-      if (!mbar_wait(&full[st], (phase >> st) & 1u, p.err, kErrWaitLoad)) s_ok = 0;
-      phase ^= 1u << st;
-      const FcStage& S = stage[st];
-      const int head = hb * 128 + h;
-      if (head < p.num_q_heads) {
-        // every item has at least one key, so every l > 0
-        // box rows: item s has m at row 2 s and l at row 2 s + 1
-        const float* mlt = &S.ml[0][0][0];
-        float M = -INFINITY;
-#pragma unroll
-        for (int s = 0; s < kFcMaxItems; ++s)
-          if (s < ns) M = fmaxf(M, mlt[(2 * s) * bi + h]);
-        float L = 0.f, w[kFcMaxItems];
-#pragma unroll
-        for (int s = 0; s < kFcMaxItems; ++s) {
-          w[s] = s < ns ? ex2_approx(mlt[(2 * s) * bi + h] - M) : 0.f;
-          L = fmaf(s < ns ? mlt[(2 * s + 1) * bi + h] : 0.f, w[s], L);
-        }
-        float den = L, alpha = 1.f;
-        if (MODE == SA_SINK_NULL_LOGIT) {
-          const float sink2 = __ldg(p.sinks + head) * kLog2e;
-          const float mp = fmaxf(M, sink2);
-          alpha = ex2_approx(M - mp);
-          den = L * alpha + ex2_approx(sink2 - mp);
-        }
-        const float inv = alpha / den;
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        const float* ot = &S.o[0][0][0];
-#pragma unroll
-        for (int s = 0; s < kFcMaxItems; ++s) {
-          if (s < ns) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              acc[e] = fmaf(w[s], ot[(s * kFcCols + half * 8 + e) * bi + h], acc[e]);
-          }
-        }
-        uint4 pk;
-        pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-        pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-        *reinterpret_cast<uint4*>(p.out + ((int64_t)q * p.num_q_heads + head) * kDv +
-                                  colblk * kFcCols + half * 8) = pk;
-        if (colblk == 0 && half == 0) p.lse[(int64_t)head * p.nq + q] = (M + log2f(L)) * kLn2;
-      }
-      __syncthreads();  // stage st is consumed
-      if (tid == 0 && s_ok && k + kFcStages < mine) issue(k + kFcStages, st);
-    }
-    unit_base += nunits;
-    __syncthreads();  // the lists are rewritten by the next round
-  }
-}
-
-// ---------------------------------------------------------------------------
-// 3b. combine: merge the (O, m, l) partials of queries with more than one item
-// and fold the sink once:
-//   O = sum_s 2^(m_s - M) O_s * alpha / (L alpha + 2^(s_h log2e - M')),
-//   M = max m_s, L = sum_s l_s 2^(m_s - M), M' = max(M, s_h log2e),
-//   alpha = 2^(M - M'), LSE = (M + log2 L) ln 2 over the listed keys only.
-// The work is cut into warp units of (query, 8 V columns, 32 heads), walked
-// round-robin by every warp of a grid of a few CTAs per SM.  Each CTA lists
-// the multi-item queries itself (256 queries at a time, in shared memory), so
-// no warp is spent on a query that needs no merge.  In a unit, lane i loads
-// the (m, l) of head i and lane (g, c) -- g = lane mod 8, c = lane / 8 -- the
-// O of heads 4 g .. + 4, columns 2 c, 2 c + 1 as float4s (eight lanes read 128
-// contiguous bytes), all in one batch; the weights meet the O values through
-// a warp-private table in shared memory, and the bf16 result goes through a
-// warp-private buffer so that each lane stores one 16-byte row segment.
-constexpr int kCombineCols = 8;
-constexpr int kCombineGroup = 8;
-constexpr int kCombineWarps = kThreads / 32;
-
-struct CombineSmem {
-  float w[kCombineWarps][kMaxSlices][32];  // 2^(m_s - M) per item and head
-  float inv[kCombineWarps][32];            // alpha / denominator per head
-  __nv_bfloat16 o[kCombineWarps][32][kCombineCols];
-  int32_t q[kThreads];
-  int32_t ns[kThreads];
-  int32_t scan[8];
-};
-
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-sparse_index_combine_kernel(const IndexParams p) {
-  __shared__ __align__(16) CombineSmem sm;
-  griddep_wait();  // the attend kernel's partials are complete
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t hs = p.head_stride;
-  const int64_t nwarps = (int64_t)gridDim.x * kCombineWarps;
-  const int64_t gw = (int64_t)blockIdx.x * kCombineWarps + warp;
-  const int ncolblk = kDv / kCombineCols;
-  const int units_per_q = ncolblk * (p.head_stride / 32);
-  const int g = lane & 7, cpair = lane >> 3;
-  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  int64_t unit_base = 0;  // units of the earlier query chunks
-  for (int qb = 0; qb < p.nq; qb += kThreads) {
-    const int qq = qb + tid;
-    const int c = qq < p.nq ? __ldcg(p.qcount + qq) : 0;
-    const int ns_q = (c + kItemKeys - 1) / kItemKeys;
-    const int act = ns_q >= 2 && ns_q >= p.combine_min_items ? 1 : 0;
-    int nact = 0;
-    const int pos = block_exclusive_sum(act, sm.scan, &nact);
-    if (act) {
-      sm.q[pos] = qq;
-      sm.ns[pos] = ns_q;
-    }
-    __syncthreads();
-    const int64_t nunits = (int64_t)nact * units_per_q;
-    // this warp's units: global unit index = gw (mod nwarps)
-    int64_t u = (gw - unit_base) % nwarps;
-    if (u < 0) u += nwarps;
-    for (; u < nunits; u += nwarps) {
-      const int a = (int)(u / units_per_q);
-      const int r = (int)(u % units_per_q);
-      const int q = sm.q[a], ns = sm.ns[a];
-      const int colblk = r % ncolblk, hg = r / ncolblk;
-      const int hm = hg * 32 + lane;    // head of this lane's (m, l)
-      const bool hm_ok = hm < p.num_q_heads;
-      const int h0 = hg * 32 + 4 * g;   // first of this lane's four O heads (< head_stride)
-      const int d = colblk * kCombineCols + 2 * cpair;
-      const float* ml = p.part_ml + (int64_t)q * p.nslices * 2 * hs + hm;
-      const float* po = p.part_o + ((int64_t)q * p.nslices * kDv + d) * hs + h0;
-      // first group: (m, l) and O together
-      float mv[kCombineGroup], lv[kCombineGroup];
-      float4 o0[kCombineGroup], o1[kCombineGroup];
-#pragma unroll
-      for (int k = 0; k < kCombineGroup; ++k) {
-        const bool live = k < ns;
-        mv[k] = live && hm_ok ? __ldcg(ml + k * 2 * hs) : -INFINITY;
-        lv[k] = live && hm_ok ? __ldcg(ml + k * 2 * hs + hs) : 0.f;
-        o0[k] = live ? __ldcg(reinterpret_cast<const float4*>(po + (int64_t)k * kDv * hs)) : z4;
-        o1[k] = live ? __ldcg(reinterpret_cast<const float4*>(po + (int64_t)k * kDv * hs + hs)) : z4;
-      }
-      // every item has at least one key, so every l > 0
-      float M = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < kCombineGroup; ++k) M = fmaxf(M, mv[k]);
-      for (int s = kCombineGroup; s < ns; ++s)
-        M = fmaxf(M, hm_ok ? __ldcg(ml + s * 2 * hs) : -INFINITY);
-      float L = 0.f;
-#pragma unroll
-      for (int k = 0; k < kCombineGroup; ++k) {
-        const float w = ex2_approx(mv[k] - M);  // 0 for absent items
-        L = fmaf(lv[k], w, L);
-        sm.w[warp][k][lane] = w;
-      }
-      for (int s = kCombineGroup; s < ns; ++s) {
-        const float w = hm_ok ? ex2_approx(__ldcg(ml + s * 2 * hs) - M) : 0.f;
-        L = fmaf(hm_ok ? __ldcg(ml + s * 2 * hs + hs) : 0.f, w, L);
-        sm.w[warp][s][lane] = w;
-      }
-      float den = L, alpha = 1.f;
-      if (MODE == SA_SINK_NULL_LOGIT) {
-        const float sink2 = hm_ok ? __ldg(p.sinks + hm) * kLog2e : 0.f;
-        const float mp = fmaxf(M, sink2);
-        alpha = ex2_approx(M - mp);
-        den = L * alpha + ex2_approx(sink2 - mp);
-      }
-      sm.inv[warp][lane] = hm_ok ? alpha / den : 0.f;
-      if (colblk == 0 && hm_ok) p.lse[(int64_t)hm * p.nq + q] = (M + log2f(L)) * kLn2;
-      __syncwarp();
-      float4 a0 = z4, a1 = z4;
-      for (int s0 = 0; s0 < ns; s0 += kCombineGroup) {
-        if (s0 > 0) {
-#pragma unroll
-          for (int k = 0; k < kCombineGroup; ++k) {
-            const bool live = s0 + k < ns;
-            const float* src = po + (int64_t)(s0 + k) * kDv * hs;
-            o0[k] = live ? __ldcg(reinterpret_cast<const float4*>(src)) : z4;
-            o1[k] = live ? __ldcg(reinterpret_cast<const float4*>(src + hs)) : z4;
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < kCombineGroup; ++k) {
-          if (s0 + k < ns) {
-            const float4 w = *reinterpret_cast<const float4*>(&sm.w[warp][s0 + k][4 * g]);
-            a0.x = fmaf(w.x, o0[k].x, a0.x);
-            a0.y = fmaf(w.y, o0[k].y, a0.y);
-            a0.z = fmaf(w.z, o0[k].z, a0.z);
-            a0.w = fmaf(w.w, o0[k].w, a0.w);
-            a1.x = fmaf(w.x, o1[k].x, a1.x);
-            a1.y = fmaf(w.y, o1[k].y, a1.y);
-            a1.z = fmaf(w.z, o1[k].z, a1.z);
-            a1.w = fmaf(w.w, o1[k].w, a1.w);
-          }
-        }
-      }
-      const float4 iv = *reinterpret_cast<const float4*>(&sm.inv[warp][4 * g]);
-      *reinterpret_cast<uint32_t*>(&sm.o[warp][4 * g + 0][2 * cpair]) = pack_bf16x2(a0.x * iv.x, a1.x * iv.x);
-      *reinterpret_cast<uint32_t*>(&sm.o[warp][4 * g + 1][2 * cpair]) = pack_bf16x2(a0.y * iv.y, a1.y * iv.y);
-      *reinterpret_cast<uint32_t*>(&sm.o[warp][4 * g + 2][2 * cpair]) = pack_bf16x2(a0.z * iv.z, a1.z * iv.z);
-      *reinterpret_cast<uint32_t*>(&sm.o[warp][4 * g + 3][2 * cpair]) = pack_bf16x2(a0.w * iv.w, a1.w * iv.w);
-      __syncwarp();
-      if (hm_ok)
-        *reinterpret_cast<uint4*>(p.out + ((int64_t)q * p.num_q_heads + hm) * kDv +
-                                  colblk * kCombineCols) =
-            *reinterpret_cast<const uint4*>(&sm.o[warp][lane][0]);
-      __syncwarp();  // sm.w / sm.o of this warp are rewritten by its next unit
-    }
-    unit_base += nunits;
-    __syncthreads();  // sm.q is rewritten by the next chunk
-  }
-}
-
 struct WorkspaceLayout {
-  size_t cidx, qcount, ml, o, total;
+  size_t cidx, qcount, done, ml, o, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1136,7 +1107,8 @@ WorkspaceLayout workspace_layout(int32_t nq, int32_t hq, int32_t topk) {
   const int nslices = (topk + kItemKeys - 1) / kItemKeys;
   w.cidx = 0;
   w.qcount = align256((size_t)nq * topk * sizeof(int32_t));
-  w.ml = w.qcount + align256((size_t)nq * sizeof(int32_t));
+  w.done = w.qcount + align256((size_t)nq * sizeof(int32_t));
+  w.ml = w.done + align256((size_t)nq * sizeof(int32_t));
   w.o = w.total = w.ml;
   if (nslices > 1) {
     const size_t hs = (size_t)head_stride(hq);
@@ -1161,10 +1133,12 @@ sa_status launch_typed(const IndexArgs& a) {
   pp.num_q_heads = a.num_q_heads;
   pp.cidx = a.topk > 0 ? reinterpret_cast<int32_t*>(ws + wl.cidx) : nullptr;
   pp.qcount = a.topk > 0 ? reinterpret_cast<int32_t*>(ws + wl.qcount) : nullptr;
+  pp.done = a.topk > 0 ? reinterpret_cast<int32_t*>(ws + wl.done) : nullptr;
   pp.out = reinterpret_cast<__nv_bfloat16*>(a.out);
   pp.lse = a.lse;
-  sparse_index_plan_kernel<<<(unsigned)a.num_queries, kThreads, 0, a.stream>>>(pp);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(sparse_index_plan_kernel, dim3((unsigned)a.num_queries),
+                                   dim3(kThreads), 0, a.stream, pp);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s plan launch: %s", fn, cudaGetErrorString(e));
   if (a.topk == 0) return SA_OK;  // every key set is empty
 
@@ -1191,64 +1165,49 @@ sa_status launch_typed(const IndexArgs& a) {
   p.part_ml = nslices > 1 ? reinterpret_cast<float*>(ws + wl.ml) : nullptr;
   p.part_o = nslices > 1 ? reinterpret_cast<float*>(ws + wl.o) : nullptr;
   p.head_stride = head_stride(a.num_q_heads);
-  p.combine_min_items = 2;
+  p.done = pp.done;
   p.err = device_error_word();
 
+  // the partials viewed as [query x item][512 columns][head_stride] (O) and
+  // [query x item x 2][head_stride] (m, l), fp32, for the TMA-fed merge
+  CUtensorMap tp, tp1, tml;
+  memset(&tp, 0, sizeof tp);
+  memset(&tp1, 0, sizeof tp1);
+  memset(&tml, 0, sizeof tml);
+  if (nslices > 1) {
+    const int64_t pitems = (int64_t)a.num_queries * nslices;
+    if (pitems * 2 >= ((int64_t)1 << 31))
+      return fail(SA_ERR_UNSUPPORTED, "%s: %lld partial items", fn, (long long)pitems);
+    const uint32_t bh = (uint32_t)std::min(128, p.head_stride);
+    const uint64_t dp[3] = {(uint64_t)p.head_stride, (uint64_t)kDv, (uint64_t)pitems};
+    const uint64_t sp[2] = {(uint64_t)p.head_stride * 4, (uint64_t)p.head_stride * 4 * kDv};
+    const uint32_t bp[3] = {bh, (uint32_t)kMergeCols, (uint32_t)kMergeGroup};
+    const uint32_t bp1[3] = {bh, (uint32_t)kMergeCols, 1u};
+    const uint64_t dm[2] = {(uint64_t)p.head_stride, (uint64_t)pitems * 2};
+    const uint64_t sm_[1] = {(uint64_t)p.head_stride * 4};
+    const uint32_t bm[2] = {bh, (uint32_t)(2 * kMergeGroup)};
+    if (!encode_tiled(&tp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.part_o, dp, sp, bp,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tiled(&tp1, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.part_o, dp, sp, bp1,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tiled(&tml, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.part_ml, dm, sm_, bm,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+      return SA_ERR_INVALID_ARG;
+  }
   const size_t smem = 1024 + (size_t)kNumSlots * kSlotBytes + 2 * (size_t)kSlabBytesQ;
   auto kern = sparse_index_fwd_kernel<MODE, FP8>;
   if (!set_dynamic_smem_once((const void*)kern, (int)smem))
     return fail(SA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(cudaGetLastError()));
-  // at most one item per (query, 256 index slots)
-  const unsigned items = (unsigned)((int64_t)a.num_queries * nslices * p.nhb);
-  e = launch_dependent(kern, dim3(items), dim3(kThreads), smem, a.stream, tq, a.kv, p);
+  // persistent: at most one CTA per SM (the shared memory allows one, and the
+  // merge waits rely on every CTA being resident), none beyond the most work
+  // there can be (one item per query and 256 index slots, per head block)
+  const int64_t max_work = (int64_t)a.num_queries * nslices * p.nhb;
+  if (max_work >= ((int64_t)1 << 31))
+    return fail(SA_ERR_UNSUPPORTED, "%s: %lld work items", fn, (long long)max_work);
+  const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(max_work, num_sms()));
+  e = launch_dependent(kern, dim3(grid), dim3(kThreads), smem, a.stream, tq, tp, tp1, tml, a.kv,
+                       p);
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));
-  if (nslices > 1) {
-    // queries with 2..8 items: TMA-fed combine over the partials viewed as
-    // [query x item][512 columns][head_stride] and the (m, l) rows as
-    // [query x item x 2][head_stride], fp32
-    const int64_t items = (int64_t)a.num_queries * nslices;
-    if (items * 2 >= ((int64_t)1 << 31))
-      return fail(SA_ERR_UNSUPPORTED, "%s: %lld partial items", fn, (long long)items);
-    const uint32_t bh = (uint32_t)std::min(128, p.head_stride);
-    CUtensorMap tp, tp1, tml;
-    const uint64_t dp[3] = {(uint64_t)p.head_stride, (uint64_t)kDv, (uint64_t)items};
-    const uint64_t sp[2] = {(uint64_t)p.head_stride * 4, (uint64_t)p.head_stride * 4 * kDv};
-    const uint32_t bp[3] = {bh, (uint32_t)kFcCols, (uint32_t)kFcMaxItems};
-    const uint32_t bp1[3] = {bh, (uint32_t)kFcCols, 1u};
-    if (!encode_tiled(&tp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.part_o, dp, sp, bp,
-                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_tiled(&tp1, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.part_o, dp, sp, bp1,
-                      CU_TENSOR_MAP_SWIZZLE_NONE))
-      return SA_ERR_INVALID_ARG;
-    const uint64_t dm[2] = {(uint64_t)p.head_stride, (uint64_t)items * 2};
-    const uint64_t sm_[1] = {(uint64_t)p.head_stride * 4};
-    const uint32_t bm[2] = {bh, (uint32_t)(2 * kFcMaxItems)};
-    if (!encode_tiled(&tml, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.part_ml, dm, sm_, bm,
-                      CU_TENSOR_MAP_SWIZZLE_NONE))
-      return SA_ERR_INVALID_ARG;
-    const int64_t max_units = (int64_t)(a.num_queries / 2) * (kDv / kFcCols) * p.nhb;
-    const unsigned g1 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(max_units, num_sms()));
-    const size_t smem_c = 128 + kFcStages * sizeof(FcStage);
-    auto kc = sparse_index_combine_tma_kernel<MODE>;
-    if (!set_dynamic_smem_once((const void*)kc, (int)smem_c))
-      return fail(SA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(cudaGetLastError()));
-    e = launch_dependent(kc, dim3(g1), dim3(kThreads), smem_c, a.stream, tp, tp1, tml, p);
-    if (e != cudaSuccess)
-      return fail(SA_ERR_CUDA, "%s combine launch: %s", fn, cudaGetErrorString(e));
-    if (nslices > kFcMaxItems) {
-      // queries with more than 8 items: warp-unit combine
-      p.combine_min_items = kFcMaxItems + 1;
-      const int64_t wunits = (int64_t)(a.num_queries / (kFcMaxItems + 1)) * (kDv / kCombineCols) *
-                             (p.head_stride / 32);
-      const int64_t per_cta = kThreads / 32;
-      const unsigned g2 = (unsigned)std::max<int64_t>(
-          1, std::min<int64_t>((wunits + per_cta - 1) / per_cta, num_sms()));
-      e = launch_dependent(sparse_index_combine_kernel<MODE>, dim3(g2), dim3(kThreads), 0,
-                           a.stream, p);
-      if (e != cudaSuccess)
-        return fail(SA_ERR_CUDA, "%s combine launch: %s", fn, cudaGetErrorString(e));
-    }
-  }
   return SA_OK;
 }
 

@@ -231,10 +231,8 @@ class IndexRunner:
         return self.counts()[0]
 
     def launches_per_call(self):
-        # plan + attend, then the combine of multi-item queries (and the
-        # fallback combine for queries with more than eight 256-key items)
-        t = self.c.topk
-        return 2 + (t > 256) + (t > 2048)
+        # plan, then the persistent attend kernel (split-KV merge included)
+        return 2
 
     def call(self, i, mode=None):
         import attention_head_sinks_gb300 as sa
