@@ -67,14 +67,17 @@ constexpr int kMaxSlices = 32;  // topk <= 32 * 256
 constexpr int kThreads = 256;
 constexpr int kMergeCols = 16;  // V columns per merge unit
 constexpr int kMergeGroup = 8;  // items whose partials are loaded at once
-constexpr int kMergeStages = 3; // merge units in flight per CTA (TMA-fed)
+constexpr int kMergeStages = 5; // merge units in flight per CTA (TMA-fed)
+constexpr int kPartChunk = 32;  // V columns sharing one fp16 scale in a partial
 
-// One merge unit's partials in shared memory: the [8 items][16 columns][128
-// heads] O box and the [8 items x (m, l)][128 heads] box, fp32, row stride the
-// tile's head count.
+// One merge unit's partials in shared memory (row stride: the tile's head
+// count): the [8 items][8 column pairs][128 heads] O box (fp16 pairs), the
+// [8 items x (m, l)][128 heads] fp32 box and the [8 items][128 heads] scale
+// exponents of the unit's 32-column chunk.
 struct __align__(128) MergeStage {
-  float o[kMergeGroup][kMergeCols][128];
+  uint32_t o[kMergeGroup][kMergeCols / 2][128];
   float ml[kMergeGroup][2][128];
+  int8_t e[kMergeGroup][128];
 };
 static_assert(kMergeStages * sizeof(MergeStage) <= kNumSlots * kSlotBytes + 2 * kSlabBytesQ,
               "merge stages reuse the attend buffers");
@@ -117,7 +120,8 @@ struct IndexParams {
   float scale_log2;
   __nv_bfloat16* out;     // [nq, hq, 512]
   float* lse;             // [hq, nq]
-  float* part_o;          // [nq][nslices][512][head_stride]
+  uint32_t* part_o;       // [nq][nslices][256 column pairs][head_stride] fp16 pairs
+  int8_t* part_e;         // [nq][nslices][16 chunks][head_stride]: O = fp16 x 2^e
   float* part_ml;         // [nq][nslices][2][head_stride]  (m, then l)
   int32_t head_stride;    // num_q_heads rounded up to 32
   int32_t* done;          // [nq]: items x head blocks finished (merge readiness)
@@ -171,6 +175,17 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
 }
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ void unpack_half2(uint32_t v, float& lo, float& hi) {
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\t"
+      "cvt.f32.f16 %1, b;\n\t}\n"
+      : "=f"(lo), "=f"(hi)
+      : "r"(v));
+}
 __device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
 __device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
@@ -192,6 +207,12 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+// Pull one tensor box into L2 (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map),
+               "r"(x), "r"(y)
+               : "memory");
 }
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
@@ -430,7 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_part,
                         const __grid_constant__ CUtensorMap tm_part1,
-                        const __grid_constant__ CUtensorMap tm_ml, const void* kv_raw,
+                        const __grid_constant__ CUtensorMap tm_ml,
+                        const __grid_constant__ CUtensorMap tm_e, const void* kv_raw,
                         const IndexParams p) {
   // bf16 cache: rows of 576 bf16; fp8 cache: rows of 576 e4m3 bytes
   const uint16_t* kv = reinterpret_cast<const uint16_t*>(kv_raw);
@@ -609,6 +631,10 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       // ---- Q slab of each S step by TMA through a two-stage ring ----------
       tma_prefetch_map(&tm_q);
       const int qrow0 = q * p.num_q_heads + hb * 128;
+      // the ring below holds two Q slabs, each refilled only once the MMAs
+      // of two steps ago have read it; pull the later slabs into L2 now so
+      // that those refills do not wait out DRAM behind the row gathers
+      for (int j = 2; j < kNumQkSlabs; ++j) tma_prefetch_l2_2d(&tm_q, step_slab(j) * kSlab, qrow0);
       int issued = 0;
       for (int j = 0; j < kNumQkSlabs; ++j) {
         const int st = j & 1;
@@ -799,7 +825,9 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     auto epilogue = [&](int tcol, int vcol, int nch) {
       __nv_bfloat16* orow = p.out + ((int64_t)q * hq + h) * kDv + vcol;
       const int64_t hs = p.head_stride;
-      float* pcol = p.part_o + (((int64_t)q * p.nslices + slice) * kDv + vcol) * hs + h;
+      const int64_t pitem = (int64_t)q * p.nslices + slice;
+      uint32_t* pcol = p.part_o + (pitem * (kDv / 2) + vcol / 2) * hs + h;
+      int8_t* ecol = p.part_e + (pitem * (kDv / kPartChunk) + vcol / kPartChunk) * hs + h;
 #pragma unroll 1
       for (int jj = 0; jj < nch; ++jj) {
         float o[32];
@@ -816,8 +844,19 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             *reinterpret_cast<uint4*>(orow + 32 * jj + 8 * g) = w;
           }
         } else if (row_valid) {
+          // fp16 with a power-of-two scale per 32-column chunk: the chunk's
+          // largest magnitude lands in [2^14, 2^15), every value keeps fp16's
+          // 11-bit relative precision, nothing overflows
+          float amax = 0.f;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pcol[(int64_t)(32 * jj + e) * hs] = o[e];
+          for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(o[e]));
+          int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127 - 14 : 0;
+          ex = max(ex, -126);
+          const float sc = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-ex
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pcol[(int64_t)(16 * jj + e) * hs] = pack_half2(o[2 * e] * sc, o[2 * e + 1] * sc);
+          ecol[(int64_t)jj * hs] = (int8_t)ex;
         }
       }
     };
@@ -919,6 +958,7 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       tma_prefetch_map(&tm_part);
       tma_prefetch_map(&tm_part1);
       tma_prefetch_map(&tm_ml);
+      tma_prefetch_map(&tm_e);
       ctl.merge_ok = 1;
     }
     __syncthreads();
@@ -990,17 +1030,21 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             // transaction; up to four items one box each, more in one box
             const int nbox = ns <= 4 ? ns : kMergeGroup;
             mbar_arrive_expect_tx(&ctl.merge_full[st],
-                                  (uint32_t)((nbox * kMergeCols + 2 * kMergeGroup) * bi * 4));
+                                  (uint32_t)((nbox * (kMergeCols / 2) + 2 * kMergeGroup) * bi * 4 +
+                                             kMergeGroup * bi));
             if (ns <= 4) {
               for (int s2 = 0; s2 < ns; ++s2)
-                tma_load_3d(&stage[st].o[0][0][0] + s2 * kMergeCols * bi, &tm_part1,
-                            &ctl.merge_full[st], hb * 128, cb * kMergeCols, q * p.nslices + s2);
+                tma_load_3d(&stage[st].o[0][0][0] + s2 * (kMergeCols / 2) * bi, &tm_part1,
+                            &ctl.merge_full[st], hb * 128, cb * (kMergeCols / 2),
+                            q * p.nslices + s2);
             } else {
               tma_load_3d(&stage[st].o[0][0][0], &tm_part, &ctl.merge_full[st], hb * 128,
-                          cb * kMergeCols, q * p.nslices);
+                          cb * (kMergeCols / 2), q * p.nslices);
             }
             tma_load_2d(&stage[st].ml[0][0][0], &tm_ml, &ctl.merge_full[st], hb * 128,
                         q * p.nslices * 2);
+            tma_load_3d(&stage[st].e[0][0], &tm_e, &ctl.merge_full[st], hb * 128,
+                        (cb * kMergeCols) / kPartChunk, q * p.nslices);
           };
           if (tid == 0)
             for (int64_t k = 0; k < mine && k < kMergeStages; ++k) issue(k, (int)k);
@@ -1016,7 +1060,8 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (ctl.merge_ok && h < p.num_q_heads) {
               // box rows: item s has m at row 2 s and l at row 2 s + 1
               const float* mlt = &stage[st].ml[0][0][0];
-              const float* ot = &stage[st].o[0][0][0];
+              const uint32_t* ot = &stage[st].o[0][0][0];
+              const int8_t* et = &stage[st].e[0][0];
               float M = -INFINITY;
 #pragma unroll
               for (int s2 = 0; s2 < kMergeGroup; ++s2)
@@ -1027,11 +1072,17 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
               for (int s2 = 0; s2 < kMergeGroup; ++s2) {
                 if (s2 < ns) {
-                  const float wk = ex2_approx(mlt[(2 * s2) * bi + h_in] - M);
-                  L = fmaf(mlt[(2 * s2 + 1) * bi + h_in], wk, L);
+                  const float dm = mlt[(2 * s2) * bi + h_in] - M;
+                  L = fmaf(mlt[(2 * s2 + 1) * bi + h_in], ex2_approx(dm), L);
+                  // the item's weight times its chunk scale 2^e
+                  const float wk = ex2_approx(dm + (float)et[s2 * bi + h_in]);
 #pragma unroll
-                  for (int e = 0; e < 8; ++e)
-                    acc[e] = fmaf(wk, ot[(s2 * kMergeCols + half * 8 + e) * bi + h_in], acc[e]);
+                  for (int i = 0; i < 4; ++i) {
+                    float lo, hi;
+                    unpack_half2(ot[(s2 * (kMergeCols / 2) + half * 4 + i) * bi + h_in], lo, hi);
+                    acc[2 * i] = fmaf(wk, lo, acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(wk, hi, acc[2 * i + 1]);
+                  }
                 }
               }
               finish(q, h, cb * kMergeCols + half * 8, M, L, acc);
@@ -1049,31 +1100,40 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int h = hb * 128 + h_in;
             if (ctl.merge_ok && h < p.num_q_heads) {
               const float* ml = p.part_ml + (int64_t)q * p.nslices * 2 * hs + h;
-              const float* po = p.part_o +
-                                ((int64_t)q * p.nslices * kDv + cb * kMergeCols + half * 8) * hs + h;
+              const uint32_t* po =
+                  p.part_o + ((int64_t)q * p.nslices * (kDv / 2) + cb * (kMergeCols / 2) + half * 4) * hs + h;
+              const int8_t* pe =
+                  p.part_e + ((int64_t)q * p.nslices * (kDv / kPartChunk) + (cb * kMergeCols) / kPartChunk) * hs + h;
               // every item has at least one key, so every l > 0
               float M = -INFINITY, L = 0.f, acc[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) acc[e] = 0.f;
               for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(ml + s2 * 2 * hs));
               for (int s0 = 0; s0 < ns; s0 += kMergeGroup) {
-                float wv[kMergeGroup], ov[kMergeGroup][8];
+                float wv[kMergeGroup];
+                uint32_t ov[kMergeGroup][4];
 #pragma unroll
                 for (int k2 = 0; k2 < kMergeGroup; ++k2) {
                   const bool live = s0 + k2 < ns;
                   const int64_t si = s0 + k2;
                   const float mk = live ? __ldcg(ml + si * 2 * hs) : -INFINITY;
                   const float lk = live ? __ldcg(ml + si * 2 * hs + hs) : 0.f;
-                  wv[k2] = ex2_approx(mk - M);  // 0 for absent items
-                  L = fmaf(lk, wv[k2], L);
+                  const float ek = live ? (float)__ldcg(pe + si * (kDv / kPartChunk) * hs) : 0.f;
+                  L = fmaf(lk, ex2_approx(mk - M), L);  // 0 for absent items
+                  wv[k2] = ex2_approx(mk - M + ek);
 #pragma unroll
-                  for (int e = 0; e < 8; ++e)
-                    ov[k2][e] = live ? __ldcg(po + (si * kDv + e) * hs) : 0.f;
+                  for (int i = 0; i < 4; ++i)
+                    ov[k2][i] = live ? __ldcg(po + (si * (kDv / 2) + i) * hs) : 0u;
                 }
 #pragma unroll
                 for (int k2 = 0; k2 < kMergeGroup; ++k2)
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) acc[e] = fmaf(wv[k2], ov[k2][e], acc[e]);
+                  for (int i = 0; i < 4; ++i) {
+                    float lo, hi;
+                    unpack_half2(ov[k2][i], lo, hi);
+                    acc[2 * i] = fmaf(wv[k2], lo, acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(wv[k2], hi, acc[2 * i + 1]);
+                  }
               }
               finish(q, h, cb * kMergeCols + half * 8, M, L, acc);
             }
@@ -1096,7 +1156,7 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 }
 
 struct WorkspaceLayout {
-  size_t cidx, qcount, done, ml, o, total;
+  size_t cidx, qcount, done, ml, e, o, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1109,11 +1169,12 @@ WorkspaceLayout workspace_layout(int32_t nq, int32_t hq, int32_t topk) {
   w.qcount = align256((size_t)nq * topk * sizeof(int32_t));
   w.done = w.qcount + align256((size_t)nq * sizeof(int32_t));
   w.ml = w.done + align256((size_t)nq * sizeof(int32_t));
-  w.o = w.total = w.ml;
+  w.e = w.o = w.total = w.ml;
   if (nslices > 1) {
     const size_t hs = (size_t)head_stride(hq);
-    w.o = w.ml + align256((size_t)nq * nslices * 2 * hs * sizeof(float));
-    w.total = w.o + (size_t)nq * nslices * kDv * hs * sizeof(float);
+    w.e = w.ml + align256((size_t)nq * nslices * 2 * hs * sizeof(float));
+    w.o = w.e + align256((size_t)nq * nslices * (kDv / kPartChunk) * hs);
+    w.total = w.o + (size_t)nq * nslices * (kDv / 2) * hs * sizeof(uint32_t);
   }
   return w;
 }
@@ -1163,32 +1224,39 @@ sa_status launch_typed(const IndexArgs& a) {
   p.out = reinterpret_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.part_ml = nslices > 1 ? reinterpret_cast<float*>(ws + wl.ml) : nullptr;
-  p.part_o = nslices > 1 ? reinterpret_cast<float*>(ws + wl.o) : nullptr;
+  p.part_o = nslices > 1 ? reinterpret_cast<uint32_t*>(ws + wl.o) : nullptr;
+  p.part_e = nslices > 1 ? reinterpret_cast<int8_t*>(ws + wl.e) : nullptr;
   p.head_stride = head_stride(a.num_q_heads);
   p.done = pp.done;
   p.err = device_error_word();
 
   // the partials viewed as [query x item][512 columns][head_stride] (O) and
   // [query x item x 2][head_stride] (m, l), fp32, for the TMA-fed merge
-  CUtensorMap tp, tp1, tml;
+  CUtensorMap tp, tp1, tml, te;
   memset(&tp, 0, sizeof tp);
   memset(&tp1, 0, sizeof tp1);
   memset(&tml, 0, sizeof tml);
+  memset(&te, 0, sizeof te);
   if (nslices > 1) {
     const int64_t pitems = (int64_t)a.num_queries * nslices;
     if (pitems * 2 >= ((int64_t)1 << 31))
       return fail(SA_ERR_UNSUPPORTED, "%s: %lld partial items", fn, (long long)pitems);
     const uint32_t bh = (uint32_t)std::min(128, p.head_stride);
-    const uint64_t dp[3] = {(uint64_t)p.head_stride, (uint64_t)kDv, (uint64_t)pitems};
-    const uint64_t sp[2] = {(uint64_t)p.head_stride * 4, (uint64_t)p.head_stride * 4 * kDv};
-    const uint32_t bp[3] = {bh, (uint32_t)kMergeCols, (uint32_t)kMergeGroup};
-    const uint32_t bp1[3] = {bh, (uint32_t)kMergeCols, 1u};
+    const uint64_t dp[3] = {(uint64_t)p.head_stride, (uint64_t)(kDv / 2), (uint64_t)pitems};
+    const uint64_t sp[2] = {(uint64_t)p.head_stride * 4, (uint64_t)p.head_stride * 4 * (kDv / 2)};
+    const uint32_t bp[3] = {bh, (uint32_t)(kMergeCols / 2), (uint32_t)kMergeGroup};
+    const uint32_t bp1[3] = {bh, (uint32_t)(kMergeCols / 2), 1u};
+    const uint64_t de[3] = {(uint64_t)p.head_stride, (uint64_t)(kDv / kPartChunk), (uint64_t)pitems};
+    const uint64_t se[2] = {(uint64_t)p.head_stride, (uint64_t)p.head_stride * (kDv / kPartChunk)};
+    const uint32_t be[3] = {bh, 1u, (uint32_t)kMergeGroup};
     const uint64_t dm[2] = {(uint64_t)p.head_stride, (uint64_t)pitems * 2};
     const uint64_t sm_[1] = {(uint64_t)p.head_stride * 4};
     const uint32_t bm[2] = {bh, (uint32_t)(2 * kMergeGroup)};
-    if (!encode_tiled(&tp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.part_o, dp, sp, bp,
+    if (!encode_tiled(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, p.part_o, dp, sp, bp,
                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_tiled(&tp1, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.part_o, dp, sp, bp1,
+        !encode_tiled(&tp1, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, p.part_o, dp, sp, bp1,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tiled(&te, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, p.part_e, de, se, be,
                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_tiled(&tml, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.part_ml, dm, sm_, bm,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -1205,8 +1273,8 @@ sa_status launch_typed(const IndexArgs& a) {
   if (max_work >= ((int64_t)1 << 31))
     return fail(SA_ERR_UNSUPPORTED, "%s: %lld work items", fn, (long long)max_work);
   const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(max_work, num_sms()));
-  e = launch_dependent(kern, dim3(grid), dim3(kThreads), smem, a.stream, tq, tp, tp1, tml, a.kv,
-                       p);
+  e = launch_dependent(kern, dim3(grid), dim3(kThreads), smem, a.stream, tq, tp, tp1, tml, te,
+                       a.kv, p);
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));
   return SA_OK;
 }

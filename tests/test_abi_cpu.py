@@ -150,15 +150,16 @@ def _a256(x):
 
 def test_sparse_index_workspace_size(lib):
     # compacted index rows (int32 [Nq, topk]), valid count and finished-item
-    # counter per query, then, with more than one 256-key item per query,
-    # (m, l) and the O partial (512 columns) fp32 per (query, item, head;
-    # head stride rounded to 32)
+    # counter per query, then, with more than one 256-key item per query, per
+    # (query, item, head; head stride rounded to 32): (m, l) fp32, one int8
+    # scale exponent per 32 V columns, and the O partial as 512 fp16 values
     head = _a256(64 * 2048 * 4) + 2 * _a256(64 * 4)
     assert lib.sa_sparse_index_workspace_size(64, 128, 512, 2048) == \
-        head + _a256(64 * 8 * 2 * 128 * 4) + 64 * 8 * 512 * 128 * 4
+        head + _a256(64 * 8 * 2 * 128 * 4) + _a256(64 * 8 * 16 * 128) + \
+        64 * 8 * 512 * 128 * 2
     assert lib.sa_sparse_index_workspace_size(3, 40, 512, 300) == \
         _a256(3 * 300 * 4) + 2 * _a256(3 * 4) + _a256(3 * 2 * 2 * 64 * 4) + \
-        3 * 2 * 512 * 64 * 4
+        _a256(3 * 2 * 16 * 64) + 3 * 2 * 512 * 64 * 2
     assert lib.sa_sparse_index_workspace_size(64, 128, 512, 256) == \
         _a256(64 * 256 * 4) + 2 * _a256(64 * 4)
     assert lib.sa_sparse_index_workspace_size(0, 128, 512, 2048) == 0
