@@ -61,7 +61,8 @@ constexpr int kStepBytes = 2 * kKVSlab;        // K (or V) of one step: 2 slabs
 constexpr int kMaxUnion = 1024;                // union blocks per tile (per metadata buffer)
 constexpr int kMaxBitmapWords = 512;           // 16384 blocks per batch row
 constexpr int kTmemCols = 512;
-constexpr int kColO = 256;
+constexpr int kSBufs = 3;                      // S / P buffers in tensor memory
+constexpr int kColO = kSBufs * 128;            // O after them
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kThreads = 384;  // warps 0..3: roles; 4..7 and 8..11: softmax parts 0 and 1
 
@@ -90,9 +91,9 @@ struct __align__(8) BlockSmemCtl {
   uint64_t k_empty[kKStages];
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_done;          // one phase per step: O += P V of that step complete
+  uint64_t s_full[kSBufs];
+  uint64_t p_full[kSBufs];
+  uint64_t o_done[2];       // [step parity]: one phase per such step, O += P V done
   uint64_t o_free;          // one phase per tile: its epilogue has read O
   uint64_t meta_full[2];    // tile metadata buffer [tile parity] written
   uint64_t meta_empty[2];   // ... and read by every role
@@ -100,7 +101,7 @@ struct __align__(8) BlockSmemCtl {
   int32_t abort_flag;       // a role's bounded wait ran out: every role stops
   int32_t sm_stop[2];       // the softmax warps' stop decision, by checkpoint parity
   int32_t nunion[2];
-  float red_m[2][2][128];   // [step parity][part][row]: row max exchange
+  float red_m[kSBufs][2][128];  // [step mod kSBufs][part][row]: row max exchange
   float red_l[2][2][128];   // [tile parity][part][row]: row sums at the end
   // per tile parity: row-local position (-1 past the last token), row-local
   // start of the token's document, KEY0_BIAS key (-1 if before the row)
@@ -200,13 +201,16 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_init(&ctl.v_full[s], 1);
       mbar_init(&ctl.v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kSBufs; ++b) {
       mbar_init(&ctl.s_full[b], 1);
       mbar_init(&ctl.p_full[b], 8);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl.meta_full[b], 1);
       mbar_init(&ctl.meta_empty[b], 11);  // 8 softmax warps, K, V, MMA
     }
-    mbar_init(&ctl.o_done, 1);
+    mbar_init(&ctl.o_done[0], 1);
+    mbar_init(&ctl.o_done[1], 1);
     mbar_init(&ctl.o_free, 8);
     ctl.abort_flag = 0;
     ctl.sm_stop[0] = ctl.sm_stop[1] = 0;
@@ -419,7 +423,7 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (ok && nsteps == 0) mbar_arrive(&ctl.q_empty);  // Q unused: release it
       auto issue_s = [&](int j) -> bool {
         const int gj = gs + j;
-        const int st = gj & 1;  // S buffer
+        const int st = gj % kSBufs;  // S buffer
         const int ks = gj % KST;
         if (!wait_or_abort(&ctl.k_full[ks], (gj / KST) & 1, kErrWaitLoad)) return false;
         tc_fence_after();
@@ -440,15 +444,18 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         mma_commit(&ctl.s_full[st]);
         return true;
       };
-      if (ok && nsteps > 0) ok = issue_s(0);
+      // S runs kSBufs - 1 steps ahead of P V: S(j + 2) goes to the pipe
+      // before P V(j), so the softmax of step j has two S's worth of tensor
+      // time to finish in before the pipe would wait for it
+      for (int j = 0; j < kSBufs - 1 && j < nsteps && ok; ++j) ok = issue_s(j);
       for (int j = 0; j < nsteps && ok; ++j) {
-        if (j + 1 < nsteps) {
-          ok = issue_s(j + 1);
+        if (j + kSBufs - 1 < nsteps) {
+          ok = issue_s(j + kSBufs - 1);
           if (!ok) break;
         }
         const int gj = gs + j;
-        const int st = gj & 1;
-        ok = wait_or_abort(&ctl.p_full[st], (gj >> 1) & 1, kErrWaitMma);
+        const int st = gj % kSBufs;
+        ok = wait_or_abort(&ctl.p_full[st], (gj / kSBufs) & 1, kErrWaitMma);
         if (!ok) break;
         // the first P V of a tile overwrites O: the previous epilogue must have read it
         if (j == 0 && n > 0) {
@@ -469,7 +476,7 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                  idesc, (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&ctl.v_empty[vs]);
-        mma_commit(&ctl.o_done);
+        mma_commit(&ctl.o_done[gj & 1]);
       }
       mbar_arrive(&ctl.meta_empty[tb]);
       if (!ok) break;
@@ -491,6 +498,12 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     // stop together or not at all: a failure is posted before a barrier and
     // every thread reads the decision right after it (the slot alternates, so
     // a later post cannot race a late reader).
+    // P V of global step k is complete.  Steps alternate between two
+    // barriers, so a barrier is never more than one phase past the step
+    // waited for: the next step on it needs this thread's P first.
+    auto wait_pv = [&](int k) -> bool {
+      return wait_or_abort(&ctl.o_done[k & 1], (uint32_t)(k >> 1) & 1u, kErrWaitMma);
+    };
     auto checkpoint = [&](bool fail) -> bool {
       if (fail) ctl.sm_stop[cp & 1] = 1;
       if (warp == 4 && lane == 0 && *abort_flag) ctl.sm_stop[cp & 1] = 1;
@@ -520,8 +533,8 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 
       for (int j = 0; j < nsteps; ++j) {
         const int gj = gs + j;
-        const int st = gj & 1;
-        ok = wait_or_abort(&ctl.s_full[st], (gj >> 1) & 1, kErrWaitMma) && ok;
+        const int st = gj % kSBufs;
+        ok = wait_or_abort(&ctl.s_full[st], (gj / kSBufs) & 1, kErrWaitMma) && ok;
         __syncwarp();
         tc_fence_after();
         // live columns of this thread's block: [clo, chi] within the block
@@ -573,7 +586,10 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
           const float m_new = need ? mx : m_use;
           const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
           if (j > 0) {
-            ok = wait_or_abort(&ctl.o_done, (gj - 1) & 1, kErrWaitMma) && ok;
+            // S(j) went to the pipe before P V(j - 2): both earlier steps
+            // may still be running
+            if (j > 1) ok = wait_pv(gj - 2) && ok;
+            ok = wait_pv(gj - 1) && ok;
             __syncwarp();
             tc_fence_after();
 #pragma unroll 1
@@ -625,14 +641,10 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (lane == 0) mbar_arrive(&ctl.p_full[st]);
       }
       if (nsteps > 0) {
-        // O is final once the last P V is done.  A parity wait only tells a
-        // phase from the one before it, and here o_done may still be two
-        // phases short (P V(last - 1) is issued after S(last), whose
-        // completion is all this thread has seen), so wait for the two phases
-        // in turn.
-        if (nsteps > 1)
-          ok = wait_or_abort(&ctl.o_done, (gs + nsteps - 2) & 1, kErrWaitMma) && ok;
-        ok = wait_or_abort(&ctl.o_done, (gs + nsteps - 1) & 1, kErrWaitMma) && ok;
+        // O is final once the last P V is done; S(last), whose completion is
+        // all this thread has seen, went to the pipe before the P V of the
+        // last kSBufs - 1 steps, so wait for each of those
+        for (int k = max(0, nsteps - kSBufs); k < nsteps; ++k) ok = wait_pv(gs + k) && ok;
         __syncwarp();
         tc_fence_after();
       }
