@@ -40,18 +40,41 @@ constexpr int kRingBudget = 220 * 1024;
 constexpr int kBufCols = 256;     // TMEM columns per buffer
 constexpr int kColO = 128;        // O within a buffer
 
+// Shared-memory layout.  A TMA copy spends about the same time on every row
+// segment it moves, whatever its width (measured: 32-byte rows cap a copy
+// stream near 20 GB/s per SM, 128-byte rows reach 37), so the rows are cut as
+// wide as the MMA operand layouts allow:
+//   Q and K (K-major): D / 64 chunks of 64 dimensions in 128-byte swizzled
+//   rows, then (D mod 64) / 16 slabs of 16 in 32-byte swizzled rows;
+//   V (the MN-major B operand of P V): atoms of 64 dimensions (128-byte
+//   swizzle) when D is a multiple of 64, else of 32 (64-byte swizzle) with the
+//   last atom zero-filled past D by the copy; P V then runs with N = VN >= D
+//   and the columns past D are ignored.
 template <int D, int G>
 struct RingShape {
   static constexpr int TQ = 128 / G;
   static constexpr int KB = TQ < 64 ? TQ : 64;
   static constexpr int NEWB = TQ / KB;
-  static constexpr int NSLAB = D / 16;
-  static constexpr int QBYTES = 128 * 32 * NSLAB;
-  static constexpr int HALF = KB * 32 * NSLAB;  // K (or V) of one block
-  static constexpr int SLOT = 2 * HALF;           // bytes per ring slot (K + V)
+  static constexpr int NC = D / 64;                 // 64-dim chunks of Q and K
+  static constexpr int NT = (D % 64) / 16;          // 16-dim tail slabs of Q and K
+  static constexpr bool V128 = (D % 64) == 0;
+  static constexpr int VW = V128 ? 64 : 32;         // dims per V atom
+  static constexpr int VA = (D + VW - 1) / VW;      // V atoms
+  static constexpr int VN = VA * VW;                // N of P V
+  static constexpr int QC = 128 * 128;              // bytes of one Q chunk
+  static constexpr int QT = 128 * 32;               // bytes of one Q tail slab
+  static constexpr int QBYTES = NC * QC + NT * QT;  // one Q stage
+  static constexpr int SLOT = KB * (NC * 128 + NT * 32 + VA * VW * 2);  // K + V of one block
   static constexpr int NR_FIT = (kRingBudget - kNQ * QBYTES) / SLOT;
   static constexpr int NR = NR_FIT > 16 ? 16 : NR_FIT;
+  // K and V are stored array by array over the whole ring: in each array
+  // slot k holds keys [k KB, (k + 1) KB), so consecutive slots are
+  // consecutive rows and one MMA can span several blocks
+  static constexpr int KC_BYTES = NR * KB * 128;    // one K chunk array
+  static constexpr int KT_BYTES = NR * KB * 32;     // one K tail array
+  static constexpr int VA_BYTES = NR * KB * VW * 2; // one V atom array
   static constexpr size_t SMEM = 1024 + (size_t)kNQ * QBYTES + (size_t)NR * SLOT;
+  static_assert(VN <= 256 - kColO, "O fits its buffer");
 };
 
 struct RingParams {
@@ -169,8 +192,10 @@ __device__ __forceinline__ int cta_item_u(const CtaItems& c, int it, const RingP
 
 template <int D, int G, int MODE>
 __global__ void __launch_bounds__(384, 1)
-window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_k,
+window_ring_kernel(const __grid_constant__ CUtensorMap tm_qc,
+                   const __grid_constant__ CUtensorMap tm_qt,
+                   const __grid_constant__ CUtensorMap tm_kc,
+                   const __grid_constant__ CUtensorMap tm_kt,
                    const __grid_constant__ CUtensorMap tm_v, const RingParams p) {
   using S = RingShape<D, G>;
   constexpr int NR = S::NR;
@@ -178,13 +203,9 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
   __shared__ RingCtl<NR> ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // K and V are stored slab-major over the whole ring: slab s of K is
-  // [NR * KB keys][16 dims], slot k holding keys [k KB, (k+1) KB) of it, so
-  // consecutive slots are consecutive rows and one MMA can span several.
-  constexpr int KSTRIDE = NR * S::KB * 32;    // bytes of one slab array
-  uint8_t* sQ = smem;                         // kNQ x [NSLAB][128][16]
-  uint8_t* sK = sQ + kNQ * S::QBYTES;         // [NSLAB][NR * KB][16]
-  uint8_t* sV = sK + S::NSLAB * KSTRIDE;      // [NSLAB][NR * KB][16]
+  uint8_t* sQ = smem;                         // kNQ x ([NC][128][64] [NT][128][16])
+  uint8_t* sK = sQ + kNQ * S::QBYTES;         // [NC][NR KB][64] [NT][NR KB][16]
+  uint8_t* sV = sK + S::NC * S::KC_BYTES + S::NT * S::KT_BYTES;  // [VA][NR KB][VW]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -221,8 +242,10 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (tid == 0) {
     // ---- TMA producer ------------------------------------------------------
-    tma_prefetch_map(&tm_q);
-    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_qc);
+    if (S::NT) tma_prefetch_map(&tm_qt);
+    tma_prefetch_map(&tm_kc);
+    if (S::NT) tma_prefetch_map(&tm_kt);
     tma_prefetch_map(&tm_v);
     ItemWalk w;
     int seq = 0, last_bl = 0, nq = 0;
@@ -233,9 +256,13 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (it >= kNQ) ok = mbar_wait(&ctl.q_empty[qs], ((it / kNQ) - 1) & 1, p.err, kErrWaitFree);
       if (!ok) break;
       mbar_arrive_expect_tx(&ctl.q_full[qs], S::QBYTES);
+      uint8_t* qst = sQ + qs * S::QBYTES;
 #pragma unroll
-      for (int s = 0; s < S::NSLAB; ++s)
-        tma_load_3d(sQ + qs * S::QBYTES + s * 128 * 32, &tm_q, &ctl.q_full[qs], 16 * s,
+      for (int c = 0; c < S::NC; ++c)
+        tma_load_3d(qst + c * S::QC, &tm_qc, &ctl.q_full[qs], 64 * c, info.g * G, info.j * S::TQ);
+#pragma unroll
+      for (int t = 0; t < S::NT; ++t)
+        tma_load_3d(qst + S::NC * S::QC + t * S::QT, &tm_qt, &ctl.q_full[qs], 64 * S::NC + 16 * t,
                     info.g * G, info.j * S::TQ);
       ++nq;
       const int bl = info.bf + p.nbt - 1;
@@ -245,11 +272,17 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (!ok) break;
         mbar_arrive_expect_tx(&ctl.kv_full[slot], S::SLOT);
 #pragma unroll
-        for (int s = 0; s < S::NSLAB; ++s) {
-          const int off = s * KSTRIDE + slot * S::KB * 32;
-          tma_load_3d(sK + off, &tm_k, &ctl.kv_full[slot], 16 * s, info.g, b * S::KB);
-          tma_load_3d(sV + off, &tm_v, &ctl.kv_full[slot], 16 * s, info.g, b * S::KB);
-        }
+        for (int c = 0; c < S::NC; ++c)
+          tma_load_3d(sK + c * S::KC_BYTES + slot * S::KB * 128, &tm_kc, &ctl.kv_full[slot],
+                      64 * c, info.g, b * S::KB);
+#pragma unroll
+        for (int t = 0; t < S::NT; ++t)
+          tma_load_3d(sK + S::NC * S::KC_BYTES + t * S::KT_BYTES + slot * S::KB * 32, &tm_kt,
+                      &ctl.kv_full[slot], 64 * S::NC + 16 * t, info.g, b * S::KB);
+#pragma unroll
+        for (int a = 0; a < S::VA; ++a)
+          tma_load_3d(sV + a * S::VA_BYTES + slot * S::KB * S::VW * 2, &tm_v, &ctl.kv_full[slot],
+                      S::VW * a, info.g, b * S::KB);
       }
       last_bl = bl;
     }
@@ -263,7 +296,7 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ---- MMA issuer --------------------------------------------------------
     ItemWalk w;
     bool ok = true;
-    const uint32_t idesc_o = idesc_bf16(128, D, true);
+    const uint32_t idesc_o = idesc_bf16(128, S::VN, true);
     auto issue_s = [&](int it, const ItemInfo& info) -> bool {
       const int b = it & 1;
       if (it >= 2 && !mbar_wait(&ctl.t_free[b], ((it >> 1) - 1) & 1, p.err, kErrWaitFree))
@@ -286,12 +319,26 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int slot0 = run == 0 ? k0 : 0;
         const uint32_t col = (uint32_t)(b * kBufCols + (run == 0 ? 0 : n1 * S::KB));
         const uint32_t idesc_s = idesc_bf16(128, nb * S::KB, false);
+        // 16 dimensions per MMA: four within each 128-byte swizzled chunk,
+        // then one per 32-byte swizzled tail slab
 #pragma unroll
-        for (int s = 0; s < S::NSLAB; ++s) {
-          const uint64_t a = smem_desc(smem_u32(qb + s * 128 * 32), 16, 256, kLayoutSw32);
-          const uint64_t bd = smem_desc(smem_u32(sK + s * KSTRIDE + slot0 * S::KB * 32), 16, 256,
-                                        kLayoutSw32);
-          mma_ss(tmem + col, a, bd, idesc_s, s > 0 ? 1u : 0u);
+        for (int c = 0; c < S::NC; ++c) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint64_t a = smem_desc(smem_u32(qb + c * S::QC) + q4 * 32, 16, 1024, kLayoutSw128);
+            const uint64_t bd = smem_desc(
+                smem_u32(sK + c * S::KC_BYTES + slot0 * S::KB * 128) + q4 * 32, 16, 1024,
+                kLayoutSw128);
+            mma_ss(tmem + col, a, bd, idesc_s, (c | q4) ? 1u : 0u);
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < S::NT; ++t) {
+          const uint64_t a = smem_desc(smem_u32(qb + S::NC * S::QC + t * S::QT), 16, 256, kLayoutSw32);
+          const uint64_t bd = smem_desc(
+              smem_u32(sK + S::NC * S::KC_BYTES + t * S::KT_BYTES + slot0 * S::KB * 32), 16, 256,
+              kLayoutSw32);
+          mma_ss(tmem + col, a, bd, idesc_s, (S::NC > 0 || t > 0) ? 1u : 0u);
         }
       }
       mma_commit(&ctl.q_empty[qs]);
@@ -317,11 +364,12 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int nrel = ahead ? S::NEWB : p.nbt;
       for (int kb = 0; kb < p.nbt; ++kb) {
         const int sq = cur.seq_bf + kb;
-        const uint8_t* vbase = sV + (sq % NR) * S::KB * 32;
+        // V rows of this block: VW * 2 bytes each, atoms VA_BYTES apart
+        const uint8_t* vbase = sV + (sq % NR) * S::KB * S::VW * 2;
 #pragma unroll
         for (int ks = 0; ks < S::KB / 16; ++ks) {
-          const uint64_t bd = smem_desc(smem_u32(vbase + ks * 16 * 32), KSTRIDE, 256,
-                                        kLayoutSw32);
+          const uint64_t bd = smem_desc(smem_u32(vbase + ks * 16 * S::VW * 2), S::VA_BYTES,
+                                        8 * S::VW * 2, S::V128 ? kLayoutSw128 : kLayoutSw64);
           mma_ts(tmem + (uint32_t)(b * kBufCols + kColO),
                  tmem + (uint32_t)(b * kBufCols + (kb * S::KB + ks * 16) / 2), bd, idesc_o,
                  (kb | ks) ? 1u : 0u);
@@ -419,20 +467,36 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_q,
 template <int D, int G, int MODE>
 sa_status launch_ring_typed(const WindowArgs& a, int nbt, int bf_off) {
   using S = RingShape<D, G>;
-  CUtensorMap tq, tk, tv;
+  // Q and K: 64-dim chunks (128-byte swizzle) and 16-dim tail slabs (32-byte
+  // swizzle); V: atoms of VW dims (the last zero-filled past D)
+  CUtensorMap tqc, tqt, tkc, tkt, tv;
   const uint64_t dq[3] = {(uint64_t)D, (uint64_t)a.num_q_heads, (uint64_t)a.total_tokens};
   const uint64_t sq[2] = {(uint64_t)D * 2, (uint64_t)a.num_q_heads * D * 2};
-  const uint32_t bq[3] = {16, (uint32_t)G, (uint32_t)S::TQ};
+  const uint32_t bqc[3] = {64, (uint32_t)G, (uint32_t)S::TQ};
+  const uint32_t bqt[3] = {16, (uint32_t)G, (uint32_t)S::TQ};
   const uint64_t dk[3] = {(uint64_t)D, (uint64_t)a.num_kv_heads, (uint64_t)a.total_tokens};
   const uint64_t sk[2] = {(uint64_t)D * 2, (uint64_t)a.num_kv_heads * D * 2};
-  const uint32_t bk[3] = {16, 1, (uint32_t)S::KB};
-  if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dq, sq, bq,
-                    CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
-      !encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dk, sk, bk,
-                    CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
-      !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dk, sk, bk,
-                    CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE))
+  const uint32_t bkc[3] = {64, 1, (uint32_t)S::KB};
+  const uint32_t bkt[3] = {16, 1, (uint32_t)S::KB};
+  const uint32_t bv[3] = {(uint32_t)S::VW, 1, (uint32_t)S::KB};
+  if (!encode_tiled(&tqc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dq, sq, bqc,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
+      !encode_tiled(&tkc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dk, sk, bkc,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
+      !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dk, sk, bv,
+                    S::V128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return SA_ERR_INVALID_ARG;
+  if (S::NT > 0) {
+    if (!encode_tiled(&tqt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dq, sq, bqt,
+                      CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
+        !encode_tiled(&tkt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dk, sk, bkt,
+                      CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE))
+      return SA_ERR_INVALID_ARG;
+  } else {
+    tqt = tqc;  // never read: no tail slabs
+    tkt = tkc;
+  }
   RingParams p;
   p.cu_seqlens = a.cu_seqlens;
   p.num_seqs = a.num_seqs;
@@ -471,7 +535,7 @@ sa_status launch_ring_typed(const WindowArgs& a, int nbt, int bf_off) {
     p.spill_per_head = p.nt - p.chunks * (int32_t)cmax;
     grid += (int)std::min<int64_t>(spare, (int64_t)p.spill_per_head * a.num_kv_heads);
   }
-  e = launch_dependent(kern, dim3(grid), dim3(384), S::SMEM, a.stream, tq, tk, tv, p);
+  e = launch_dependent(kern, dim3(grid), dim3(384), S::SMEM, a.stream, tqc, tqt, tkc, tkt, tv, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess)
     return fail(SA_ERR_CUDA, "sa_varlen_window_fwd launch: %s", cudaGetErrorString(e));
