@@ -987,11 +987,17 @@ class Bench:
     def timed(self, mode, steps):
         """The contract's timed region: ``steps`` calls through the public
         API, bracketed by barrier + synchronize, CUDA events on the launching
-        stream at both ends; nothing else is enqueued in between.  Returns
-        the slowest rank's milliseconds."""
+        stream at both ends; nothing else is enqueued in between.  The calls
+        are queued behind a device-side sleep recorded before the first event,
+        so that the host's enqueue time of the first calls never shows as idle
+        device time inside the region (it is measured by the end-to-end leg).
+        Returns the slowest rank's milliseconds."""
         torch = self.torch
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         self.barrier()
+        sleep = getattr(torch.cuda, "_sleep", None)
+        if sleep is not None:  # about 30 us of host time per queued call
+            sleep(int(2.0e9 * (0.002 + min(steps, 2000) * 30e-6)))
         e0.record()
         for i in range(steps):
             self.r.call(i, mode)
@@ -1151,6 +1157,9 @@ def main():
     ap.add_argument("--no-workloads", action="store_true",
                     help="measure only --workload (no per-configuration entries)")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--only-timed", action="store_true",
+                    help="warm-up and the timed region only (for profiler launch lists): no "
+                         "sink-cost, isolated-launch, end-to-end, sustained or per-workload legs")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.steps is None:
@@ -1177,18 +1186,23 @@ def main():
     b.warm(args.warmup)
     step_ms = b.timed(runner.mode, args.steps) / args.steps
     call_us = step_ms * 1000.0
-    sc = b.sink_cost(args.steps)
-    e2e = b.e2e(args.e2e_steps)
-    sustained = b.sustained(SUSTAINED_S)
+    if args.only_timed:
+        sc = {"sink_cost": None, "sink_cost_isolated": None, "launch_us_isolated": None,
+              "launch_us_isolated_sinks_disabled": None}
+        e2e = sustained = None
+    else:
+        sc = b.sink_cost(args.steps)
+        e2e = b.e2e(args.e2e_steps)
+        sustained = b.sustained(SUSTAINED_S)
 
     src_hash = kernel_source_hash(runner.source)
     traffic = recorded_traffic(args.workload, src_hash)
     roof, other = b.roofline(call_us, traffic, src_hash)
     roof["launch_us_isolated"] = sc["launch_us_isolated"]
-    roof["sustained_call_us"] = sustained["value"]
+    roof["sustained_call_us"] = sustained["value"] if sustained else None
 
     workloads = {}
-    if not args.no_workloads and args.workload == "vision_window_16384tok":
+    if not (args.no_workloads or args.only_timed) and args.workload == "vision_window_16384tok":
         del b
         torch.cuda.empty_cache()
         for name, steps in EXTRA_WORKLOADS:
@@ -1241,7 +1255,7 @@ def main():
     }
     if workloads:
         line["workloads"] = workloads
-    if not args.no_cpu_baseline:
+    if not (args.no_cpu_baseline or args.only_timed):
         line["cpu_baseline"] = cpu_baseline(runner)
     print(json.dumps(line), flush=True)
     if dist is not None:
