@@ -23,13 +23,15 @@
 //     no CTA is launched without work).  Per (item, block of 128 heads):
 //       S = Q K^T      M = 128 heads, N = item keys (rounded to 16), K = 576
 //                      in nine 64-wide slabs;
-//       O_half = P V   twice, N = 256 V columns each, K = the item's keys.
+//       O = P V        in three parts of 256, 128 and 128 V columns (tensor
+//                      memory holds S and one 128 x 512 fp32 O only in
+//                      part), K = the item's keys.
 //     A query with a single item is finished there (sink fold, bf16 O, LSE).
 //     Otherwise the item's (O, m, l) partial goes to the workspace and the
 //     query's completion counter is raised.  Once a CTA has no items left it
 //     merges: units of (query with several items, block of 128 heads, 16 V
-//     columns) are dealt round-robin over the CTAs; a unit waits (bounded)
-//     for its query's counter, then merges the partials by their LSE weights
+//     columns) are split into one contiguous range per CTA; a unit waits
+//     (bounded) for its query's counter, then merges the partials by their LSE weights
 //     and folds the sink once.  Every CTA of the grid is resident (one per
 //     SM), and a CTA merges only after finishing its own items, so every
 //     wait ends.
@@ -65,22 +67,35 @@ constexpr int kColS = 0;
 constexpr int kColO = 256;
 constexpr int kMaxSlices = 32;  // topk <= 32 * 256
 constexpr int kThreads = 256;
-constexpr int kMergeCols = 16;  // V columns per merge unit
+constexpr int kMergeCols = 32;  // V columns per merge unit
+constexpr int kMergeSegs = kMergeCols / 16;  // 8-column segments per merge thread
+static_assert(kMergeCols % 16 == 0 && kMergeCols <= 32, "a merge unit lies inside one scale chunk");
 constexpr int kMergeGroup = 8;  // items whose partials are loaded at once
-constexpr int kMergeStages = 5; // merge units in flight per CTA (TMA-fed)
+constexpr int kMergeStages = 3; // merge units in flight per CTA (TMA-fed)
 constexpr int kPartChunk = 32;  // V columns sharing one fp16 scale in a partial
 
 // One merge unit's partials in shared memory (row stride: the tile's head
-// count): the [8 items][8 column pairs][128 heads] O box (fp16 pairs), the
-// [8 items x (m, l)][128 heads] fp32 box and the [8 items][128 heads] scale
-// exponents of the unit's 32-column chunk.
+// count): the [8 items][8 column pairs][128 heads] O box (fp16 pairs) and the
+// [8 items][128 heads] scale exponents of the unit's 32-column chunk.
 struct __align__(128) MergeStage {
   uint32_t o[kMergeGroup][kMergeCols / 2][128];
-  float ml[kMergeGroup][2][128];
   int8_t e[kMergeGroup][128];
 };
-static_assert(kMergeStages * sizeof(MergeStage) <= kNumSlots * kSlotBytes + 2 * kSlabBytesQ,
-              "merge stages reuse the attend buffers");
+// The [8 items x (m, l)][128 heads] fp32 box of a (query, head block): loaded
+// once per CTA for the run of its units that share it, into one of two
+// buffers.
+struct __align__(128) MergeMl {
+  float ml[kMergeGroup][2][128];
+};
+constexpr int kUnitsPerHb = kDv / kMergeCols;  // merge units per (query, head block)
+// Two ml buffers are enough: a CTA's units are one contiguous range, so a
+// (query, head block) that is neither its first nor its last one has all
+// kUnitsPerHb of its units in the range, more than the units in flight.
+static_assert(kMergeStages < kUnitsPerHb, "ml buffer reuse needs runs longer than the stages");
+constexpr size_t kMergeSmem =
+    kMergeStages * sizeof(MergeStage) + 2 * sizeof(MergeMl) + kThreads * sizeof(int32_t);
+static_assert(kMergeSmem <= kNumSlots * kSlotBytes + 2 * kSlabBytesQ,
+              "merge stages, ml buffers and item counts reuse the attend buffers");
 
 // S step j: slab of Q/K and the slot it sits in (0..3 = R0..R3, 4 = K0,
 // 5 = K1).  The ring slabs come first so that the ring refills overlap the
@@ -142,6 +157,7 @@ struct __align__(8) IndexSmemCtl {
   uint32_t tmem_base;
   int32_t item_q, item_s, item_n, item_nitems;
   int32_t merge_ok;
+  int32_t merge_range[2];    // this CTA's merge units [first, end) of a chunk
   uint64_t merge_full[kMergeStages];
   int32_t scan_f[8], scan_p[8];
   int32_t kidx[kItemKeys];  // the item's key rows
@@ -727,13 +743,18 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     // fp8 maxima are already in the log2 domain
     const float m = fmaxf(red.m[0][row], red.m[1][row]) * (FP8 ? 1.f : c2);
     {
-      // pass 2: P = 2^(s c2 - m) (bf16, written over S: key columns [k0, k0 +
-      // 128) go to TMEM columns [k0, k0 + 64), inside this thread's half) and
-      // the row sum
+      // pass 2: P = 2^(s c2 - m) (bf16, written over S inside this thread's
+      // half) and the row sum.  Key chunk ch of 32 keys goes to TMEM columns
+      // pcol0 + 16 ch: part 0 fills [0, 64) in ascending chunk order, part 1
+      // fills [192, 256) in descending order, so every store lands on
+      // columns this thread has already read, and [64, 192) is left free
+      // as one 128-column block for an O part
       const uint64_t c2c2 = f2_pack(c2, c2), nmnm = f2_pack(-m, -m);
+      const int pcol0 = part == 0 ? 0 : 192;
       uint64_t lp[4] = {0, 0, 0, 0};
 #pragma unroll 1
-      for (int ch = 0; ch < nch; ++ch) {
+      for (int i = 0; i < nch; ++i) {
+        const int ch = part == 0 ? i : nch - 1 - i;
         float v[32];
         tmem_ld32(lane_base + kColS + k0 + 32 * ch, v);
         tmem_wait_ld();
@@ -763,7 +784,7 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             pk[e >> 1] = pack_bf16x2(x0, x1);
           }
         }
-        tmem_st16(lane_base + kColS + k0 + 16 * ch, pk);
+        tmem_st16(lane_base + kColS + pcol0 + 16 * ch, pk);
       }
       const uint64_t s01 = f2_add(lp[0], lp[1]), s23 = f2_add(lp[2], lp[3]);
       const uint64_t s = f2_add(s01, s23);
@@ -787,9 +808,8 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ---- O = P V in three parts (thread 0 issues), each with its epilogue ----
     // After S the resident slabs are 0..3 (R0..R3) and 6, 7 (K0, K1):
     //   A:  V columns 0..255   <- R0..R3, N = 256, into TMEM [256, 512);
-    //   B1: V columns 384..511 <- K0, K1, N = 64 each, into the S columns
-    //       the softmax left free, [64, 128) and [192, 256) (P sits in
-    //       [0, 64) and [128, 192));
+    //   B1: V columns 384..511 <- K0, K1, N = 128, into the S columns the
+    //       softmax left free, [64, 192) (P sits in [0, 64) and [192, 256));
     //   B2: V columns 256..383 <- slabs 4, 5 gathered again over R2, R3 once
     //       A has read them, N = 128, into TMEM [256, 384) once the
     //       epilogue of A has read it.
@@ -800,8 +820,8 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint32_t vb = slot_u32(first_slot);
       for (int kk = 0; kk < npad / 16; ++kk) {
         // P of keys [16 kk, 16 kk + 16): TMEM column 8 kk (keys < 128) or
-        // 128 + 8 (kk - 8)
-        const uint32_t pa = tmem + kColS + (kk < 8 ? kk * 8 : 128 + (kk - 8) * 8);
+        // 192 + 8 (kk - 8)
+        const uint32_t pa = tmem + kColS + (kk < 8 ? kk * 8 : 192 + (kk - 8) * 8);
         const uint64_t b = smem_desc(vb + kk * 16 * 128, kSlotBytes, 1024, kLayoutSw128);
         mma_ts(tmem + col, pa, b, idesc, kk > 0 ? 1u : 0u);
       }
@@ -811,8 +831,7 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc_fence_after();
         issue_pv(0, kColO, 256);
         mma_commit(&ctl.oa_full);
-        issue_pv(4, kColS + 64, 64);
-        issue_pv(5, kColS + 192, 64);
+        issue_pv(4, kColS + 64, 128);
         mma_commit(&ctl.ob1_full);
       } else {
         mbar_arrive(&ctl.oa_full);
@@ -900,7 +919,7 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     ok = mbar_wait(&ctl.ob1_full, 0, p.err, kErrWaitMma) && ok;
     __syncwarp();
     tc_fence_after();
-    epilogue(kColS + 64 + part * 128, 384 + part * 64, 2);
+    epilogue(kColS + 64 + part * 64, 384 + part * 64, 2);
     ok = mbar_wait(&ctl.ob2_full, 0, p.err, kErrWaitMma) && ok;
     __syncwarp();
     tc_fence_after();
@@ -931,24 +950,34 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   // ---- split-KV merge -------------------------------------------------------------
   // Units of (query with several items, block of 128 heads, 16 V columns),
-  // dealt round-robin over the CTAs, 256 queries at a time; a unit waits
-  // (bounded) until every item of its query is counted.  Thread t merges
-  // head t mod 128 of the unit's head block, V columns 8 (t / 128) .. + 8:
+  // 256 queries at a time, split into one contiguous range per CTA with
+  // about equal partial bytes per CTA (a unit weighs the items it loads), so
+  // a CTA's units mostly share a query: it waits for one counter and loads
+  // one (m, l) box per run, not one per unit.  A unit waits (bounded) until
+  // every item of its query is counted.  Thread t merges head t mod 128 of
+  // the unit's head block, half t / 128 of the unit's V columns:
   //   O = sum_s 2^(m_s - M) O_s * alpha / (L alpha + 2^(s_h log2e - M')),
   //   M = max m_s, L = sum_s l_s 2^(m_s - M), M' = max(M, s_h log2e),
   //   alpha = 2^(M - M'), LSE = (M + log2 L) ln 2 over the listed keys only.
-  // Queries of at most eight items: thread 0 loads each unit with two TMA
-  // copies into one of three shared-memory stages (the attend buffers, free
-  // now), so three units' reads are in flight without register cost.  More
-  // items: plain loads, eight items at a time.
+  // Queries of at most eight items: lane 0 of warp st loads the units of
+  // stage st (one issuing thread per stage) by TMA into one of kMergeStages
+  // shared-memory stages (the attend buffers, free now): each unit's O and
+  // scale boxes, and the (m, l) box once per run of units of one (query,
+  // head block), so several units' reads are in flight without register
+  // cost.  More items: plain loads, eight items at a time.
   {
     const int h_in = tid & 127, half = tid >> 7;
     const int64_t hs = p.head_stride;
     const int bi = hs < 128 ? (int)hs : 128;  // heads per TMA box row
-    constexpr int kUnitsPerHb = kDv / kMergeCols;
     const int64_t per_q = (int64_t)p.nhb * kUnitsPerHb;
     const int64_t G = gridDim.x;
     MergeStage* stage = reinterpret_cast<MergeStage*>(s_slot);
+    MergeMl* s_ml = reinterpret_cast<MergeMl*>(s_slot + kMergeStages * sizeof(MergeStage));
+    // item counts of the chunk's merged queries (ctl.kidx holds the queries)
+    int32_t* s_mns = reinterpret_cast<int32_t*>(s_ml + 2);
+    int last_ready = -1;  // the last query this thread found complete
+    // the stage this thread fills (lane 0 of warps 0 .. kMergeStages - 1), or -1
+    const int lane0_of_stage = (tid & 31) == 0 && tid / 32 < kMergeStages ? tid / 32 : -1;
     // the stages overlay buffers this CTA wrote through the generic proxy
     // (the softmax exchange); order those writes before the copies' writes
     fence_proxy_async();
@@ -997,22 +1026,40 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint32_t phase = 0;
     // pass 0: queries of 2..8 items (TMA-fed); pass 1: more than 8 (plain loads)
     for (int pass = 0; pass < 2; ++pass) {
-      int64_t ubase = 0;
       for (int qc = 0; qc < p.nq; qc += kThreads) {
         const int qq = qc + tid;
         const int nsq = qq < p.nq ? (__ldcg(p.qcount + qq) + kItemKeys - 1) / kItemKeys : 0;
         const int act = (pass == 0 ? (nsq >= 2 && nsq <= kMergeGroup) : nsq > kMergeGroup) ? 1 : 0;
         int nact = 0;
         const int pos = block_exclusive_sum(act, ctl.scan_f, &nact);
-        if (act) ctl.kidx[pos] = qq;
-        __syncthreads();
+        if (act) {
+          ctl.kidx[pos] = qq;
+          s_mns[pos] = nsq;
+        }
+        // a unit of this query weighs the items its copies load; CTA b takes
+        // the units whose weight starts in [W b / G, W (b + 1) / G)
+        const int wq = act ? 1 : 0;
+        int wtot = 0;
+        const int wpre = block_exclusive_sum(wq, ctl.scan_p, &wtot);
         const int64_t nunits = (int64_t)nact * per_q;
-        int64_t first = ((int64_t)blockIdx.x - ubase) % G;
-        if (first < 0) first += G;
-        const int64_t mine = first < nunits ? (nunits - first + G - 1) / G : 0;
-        auto unit_of = [&](int64_t k, int& q, int& hb, int& cb) {
-          const int64_t u = first + k * G;
+        const int64_t W = per_q * wtot;
+        const int64_t xb = W * blockIdx.x / G, xe = W * (blockIdx.x + 1) / G;
+        if (act) {
+          const int64_t lo = per_q * wpre, hi = lo + per_q * wq;
+          if (xb >= lo && xb < hi) ctl.merge_range[0] = (int)(pos * per_q + (xb - lo + wq - 1) / wq);
+          if (xe >= lo && xe < hi) ctl.merge_range[1] = (int)(pos * per_q + (xe - lo + wq - 1) / wq);
+        }
+        if (tid == 0) {
+          if (xb >= W) ctl.merge_range[0] = (int)nunits;
+          if (xe >= W) ctl.merge_range[1] = (int)nunits;
+        }
+        __syncthreads();
+        const int64_t first = ctl.merge_range[0];
+        const int64_t mine = ctl.merge_range[1] - first;
+        auto unit_of = [&](int64_t k, int& q, int& ns, int& hb, int& cb) {
+          const int64_t u = first + k;
           q = ctl.kidx[(int)(u / per_q)];
+          ns = s_mns[(int)(u / per_q)];
           const int r = (int)(u % per_q);
           hb = r / kUnitsPerHb;
           cb = r % kUnitsPerHb;
@@ -1020,17 +1067,26 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (pass == 0) {
           // thread 0: unit k's two copies into stage st, once its query is ready
           auto issue = [&](int64_t k, int st) {
-            int q, hb, cb;
-            unit_of(k, q, hb, cb);
-            const int ns = (__ldcg(p.qcount + q) + kItemKeys - 1) / kItemKeys;
-            if (!wait_ready(q, ns)) ctl.merge_ok = 0;
-            // the partials were written through the generic proxy by other SMs
-            asm volatile("fence.proxy.async.global;" ::: "memory");
+            int q, ns, hb, cb;
+            unit_of(k, q, ns, hb, cb);
+            if (q != last_ready) {
+              if (!wait_ready(q, ns)) ctl.merge_ok = 0;
+              // the partials were written through the generic proxy by
+              // other SMs; this orders them before every later copy
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+              last_ready = q;
+            }
+            // the (m, l) box once per run of units of one (query, head
+            // block), into the buffer of the run's parity in the range
+            const int64_t u = first + k;
+            const bool load_ml = k == 0 || u % kUnitsPerHb == 0;
+            const int iss_ml = (int)((u / kUnitsPerHb - first / kUnitsPerHb) & 1);
             // full boxes (out-of-range parts zero-filled) count in the
             // transaction; up to four items one box each, more in one box
             const int nbox = ns <= 4 ? ns : kMergeGroup;
             mbar_arrive_expect_tx(&ctl.merge_full[st],
-                                  (uint32_t)((nbox * (kMergeCols / 2) + 2 * kMergeGroup) * bi * 4 +
+                                  (uint32_t)((nbox * (kMergeCols / 2) + (load_ml ? 2 * kMergeGroup : 0)) *
+                                                 bi * 4 +
                                              kMergeGroup * bi));
             if (ns <= 4) {
               for (int s2 = 0; s2 < ns; ++s2)
@@ -1041,34 +1097,38 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
               tma_load_3d(&stage[st].o[0][0][0], &tm_part, &ctl.merge_full[st], hb * 128,
                           cb * (kMergeCols / 2), q * p.nslices);
             }
-            tma_load_2d(&stage[st].ml[0][0][0], &tm_ml, &ctl.merge_full[st], hb * 128,
-                        q * p.nslices * 2);
+            if (load_ml)
+              tma_load_2d(&s_ml[iss_ml].ml[0][0][0], &tm_ml, &ctl.merge_full[st], hb * 128,
+                          q * p.nslices * 2);
             tma_load_3d(&stage[st].e[0][0], &tm_e, &ctl.merge_full[st], hb * 128,
                         (cb * kMergeCols) / kPartChunk, q * p.nslices);
           };
-          if (tid == 0)
-            for (int64_t k = 0; k < mine && k < kMergeStages; ++k) issue(k, (int)k);
+          // stage st is filled by lane 0 of warp st: one issuing thread per
+          // stage, each with its own copies in flight
+          if (lane0_of_stage >= 0 && lane0_of_stage < mine) issue(lane0_of_stage, lane0_of_stage);
           for (int64_t k = 0; k < mine; ++k) {
             const int st = (int)(k % kMergeStages);
-            int q, hb, cb;
-            unit_of(k, q, hb, cb);
-            const int ns = (__ldcg(p.qcount + q) + kItemKeys - 1) / kItemKeys;
+            int q, ns, hb, cb;
+            unit_of(k, q, ns, hb, cb);
             if (!mbar_wait(&ctl.merge_full[st], (phase >> st) & 1u, p.err, kErrWaitLoad))
               ctl.merge_ok = 0;
             phase ^= 1u << st;
+            const int con_ml = (int)(((first + k) / kUnitsPerHb - first / kUnitsPerHb) & 1);
             const int h = hb * 128 + h_in;
             if (ctl.merge_ok && h < p.num_q_heads) {
               // box rows: item s has m at row 2 s and l at row 2 s + 1
-              const float* mlt = &stage[st].ml[0][0][0];
+              const float* mlt = &s_ml[con_ml].ml[0][0][0];
               const uint32_t* ot = &stage[st].o[0][0][0];
               const int8_t* et = &stage[st].e[0][0];
               float M = -INFINITY;
 #pragma unroll
               for (int s2 = 0; s2 < kMergeGroup; ++s2)
                 if (s2 < ns) M = fmaxf(M, mlt[(2 * s2) * bi + h_in]);
-              float L = 0.f, acc[8];
+              float L = 0.f, acc[kMergeSegs][8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+              for (int g = 0; g < kMergeSegs; ++g)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
 #pragma unroll
               for (int s2 = 0; s2 < kMergeGroup; ++s2) {
                 if (s2 < ns) {
@@ -1077,38 +1137,48 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                   // the item's weight times its chunk scale 2^e
                   const float wk = ex2_approx(dm + (float)et[s2 * bi + h_in]);
 #pragma unroll
-                  for (int i = 0; i < 4; ++i) {
+                  for (int i = 0; i < 4 * kMergeSegs; ++i) {
                     float lo, hi;
-                    unpack_half2(ot[(s2 * (kMergeCols / 2) + half * 4 + i) * bi + h_in], lo, hi);
-                    acc[2 * i] = fmaf(wk, lo, acc[2 * i]);
-                    acc[2 * i + 1] = fmaf(wk, hi, acc[2 * i + 1]);
+                    unpack_half2(ot[(s2 * (kMergeCols / 2) + half * 4 * kMergeSegs + i) * bi + h_in],
+                                 lo, hi);
+                    acc[i >> 2][2 * (i & 3)] = fmaf(wk, lo, acc[i >> 2][2 * (i & 3)]);
+                    acc[i >> 2][2 * (i & 3) + 1] = fmaf(wk, hi, acc[i >> 2][2 * (i & 3) + 1]);
                   }
                 }
               }
-              finish(q, h, cb * kMergeCols + half * 8, M, L, acc);
+#pragma unroll
+              for (int g = 0; g < kMergeSegs; ++g)
+                finish(q, h, cb * kMergeCols + (half * kMergeSegs + g) * 8, M, L, acc[g]);
             }
             __syncthreads();  // stage st is consumed
-            if (tid == 0 && k + kMergeStages < mine) issue(k + kMergeStages, st);
+            if (lane0_of_stage == st && k + kMergeStages < mine) issue(k + kMergeStages, st);
           }
         } else {
           for (int64_t k = 0; k < mine; ++k) {
-            int q, hb, cb;
-            unit_of(k, q, hb, cb);
-            const int ns = (__ldcg(p.qcount + q) + kItemKeys - 1) / kItemKeys;
-            if (tid == 0 && !wait_ready(q, ns)) ctl.merge_ok = 0;
+            int q, ns, hb, cb;
+            unit_of(k, q, ns, hb, cb);
+            if (tid == 0 && q != last_ready) {
+              if (!wait_ready(q, ns)) ctl.merge_ok = 0;
+              last_ready = q;
+            }
             __syncthreads();
             const int h = hb * 128 + h_in;
             if (ctl.merge_ok && h < p.num_q_heads) {
               const float* ml = p.part_ml + (int64_t)q * p.nslices * 2 * hs + h;
-              const uint32_t* po =
-                  p.part_o + ((int64_t)q * p.nslices * (kDv / 2) + cb * (kMergeCols / 2) + half * 4) * hs + h;
               const int8_t* pe =
                   p.part_e + ((int64_t)q * p.nslices * (kDv / kPartChunk) + (cb * kMergeCols) / kPartChunk) * hs + h;
               // every item has at least one key, so every l > 0
-              float M = -INFINITY, L = 0.f, acc[8];
+              float M = -INFINITY, L = 0.f;
+              for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(ml + s2 * 2 * hs));
+              for (int s2 = 0; s2 < ns; ++s2)
+                L = fmaf(__ldcg(ml + s2 * 2 * hs + hs), ex2_approx(__ldcg(ml + s2 * 2 * hs) - M), L);
+#pragma unroll 1
+              for (int g = 0; g < kMergeSegs; ++g) {
+              const uint32_t* po = p.part_o + ((int64_t)q * p.nslices * (kDv / 2) +
+                                               cb * (kMergeCols / 2) + (half * kMergeSegs + g) * 4) * hs + h;
+              float acc[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-              for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(ml + s2 * 2 * hs));
               for (int s0 = 0; s0 < ns; s0 += kMergeGroup) {
                 float wv[kMergeGroup];
                 uint32_t ov[kMergeGroup][4];
@@ -1117,10 +1187,8 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const bool live = s0 + k2 < ns;
                   const int64_t si = s0 + k2;
                   const float mk = live ? __ldcg(ml + si * 2 * hs) : -INFINITY;
-                  const float lk = live ? __ldcg(ml + si * 2 * hs + hs) : 0.f;
                   const float ek = live ? (float)__ldcg(pe + si * (kDv / kPartChunk) * hs) : 0.f;
-                  L = fmaf(lk, ex2_approx(mk - M), L);  // 0 for absent items
-                  wv[k2] = ex2_approx(mk - M + ek);
+                  wv[k2] = ex2_approx(mk - M + ek);  // 0 for absent items
 #pragma unroll
                   for (int i = 0; i < 4; ++i)
                     ov[k2][i] = live ? __ldcg(po + (si * (kDv / 2) + i) * hs) : 0u;
@@ -1135,13 +1203,13 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     acc[2 * i + 1] = fmaf(wv[k2], hi, acc[2 * i + 1]);
                   }
               }
-              finish(q, h, cb * kMergeCols + half * 8, M, L, acc);
+              finish(q, h, cb * kMergeCols + (half * kMergeSegs + g) * 8, M, L, acc);
+              }
             }
             __syncthreads();  // ctl.merge_ok may be rewritten by the next unit
           }
         }
-        ubase += nunits;
-        __syncthreads();  // ctl.kidx is rewritten by the next chunk
+        __syncthreads();  // ctl.kidx and s_mns are rewritten by the next chunk
       }
     }
   }
