@@ -324,6 +324,7 @@ sparse_index_plan_kernel(const PlanParams p) {
 // ctl.item_* (q = -1 past the last item).  Both contain __syncthreads.
 struct ItemScan {
   int pre_f, pre_p, nfull, npart, tot_f, tot_p;
+  int cnt0, cnt1;  // counts of this thread's first two queries (lookup reuses them)
 };
 
 __device__ ItemScan scan_items(const IndexParams& p, IndexSmemCtl& ctl) {
@@ -332,9 +333,13 @@ __device__ ItemScan scan_items(const IndexParams& p, IndexSmemCtl& ctl) {
   ItemScan sc;
   sc.nfull = 0;
   sc.npart = 0;
+  sc.cnt0 = 0;
+  sc.cnt1 = 0;
   for (int i = 0; i < K; ++i) {
     const int qq = tid * K + i;
     const int c = qq < p.nq ? __ldcg(p.qcount + qq) : 0;
+    if (i == 0) sc.cnt0 = c;
+    if (i == 1) sc.cnt1 = c;
     sc.nfull += c / kItemKeys;
     sc.npart += (c % kItemKeys) != 0 ? 1 : 0;
   }
@@ -357,7 +362,7 @@ __device__ void lookup_item(const IndexParams& p, const ItemScan& sc, int item,
     int acc = pre;
     for (int i = 0; i < K; ++i) {
       const int qq = tid * K + i;
-      const int c = __ldcg(p.qcount + qq);
+      const int c = i == 0 ? sc.cnt0 : i == 1 ? sc.cnt1 : __ldcg(p.qcount + qq);
       const int f = c / kItemKeys, r = c % kItemKeys;
       const int here = heavy ? f : (r != 0 ? 1 : 0);
       if (target < acc + here) {
