@@ -233,8 +233,10 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
-__device__ __forceinline__ void bar_gather() {  // the four gatherer warps only
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+// Named barrier of the gatherer warps (the last N / 32 warps of the CTA).
+template <int N = 128>
+__device__ __forceinline__ void bar_gather() {
+  asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -453,14 +455,14 @@ __device__ __noinline__ void convert_slab_fp8(uint32_t dst, int npad, int r0, in
   }
 }
 
-// Gather 16-byte chunk c of slab `slab` of rows r0, r0 + 16, ... (< npad) into
-// the 128-byte-swizzled [npad][64] slot at dst; rows past n are zero-filled.
+// Gather 16-byte chunk c of slab `slab` of rows r0, r0 + step, ... (< npad)
+// into the 128-byte-swizzled [npad][64] slot at dst; rows past n are
+// zero-filled.
 __device__ __forceinline__ void gather_slab(uint32_t dst, const uint16_t* kv,
-                                            const int32_t* kidx, int iters, int n, int r0,
-                                            int c, int slab) {
+                                            const int32_t* kidx, int npad, int step, int n,
+                                            int r0, int c, int slab) {
 #pragma unroll 4
-  for (int k = 0; k < iters; ++k) {
-    const int r = r0 + 16 * k;
+  for (int r = r0; r < npad; r += step) {
     const bool live = r < n;
     const uint16_t* src = kv + (live ? (int64_t)kidx[r] * kDqk + slab * kSlab + c * 8 : 0);
     cp_async16(dst + r * 128 + ((c ^ (r & 7)) << 4), src, live ? 16u : 0u);
@@ -475,6 +477,13 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_ml,
                         const __grid_constant__ CUtensorMap tm_e, const void* kv_raw,
                         const IndexParams p) {
+  // Warps that gather latent rows during S: six for the bf16 cache (every
+  // warp but the two that hold the MMA and Q-load threads; more warps issue
+  // 16-byte copies faster), four for the fp8 cache (its staging and
+  // conversion are laid out for 128 threads).
+  constexpr int kGatherWarps = FP8 ? 4 : 6;
+  constexpr int kGatherThreads = 32 * kGatherWarps;
+  static_assert(kGatherThreads % 8 == 0 && kGatherThreads <= kThreads - 64, "");
   // bf16 cache: rows of 576 bf16; fp8 cache: rows of 576 e4m3 bytes
   const uint16_t* kv = reinterpret_cast<const uint16_t*>(kv_raw);
   const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(kv_raw);
@@ -508,10 +517,10 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (tid == 0) {
     // every barrier starts each item at phase 0 (the previous item's
     // arrivals have all landed: its last waits saw them)
-    for (int i = 0; i < 4; ++i) mbar_init(&ctl.res_full[i], 128);
-    mbar_init(&ctl.res2_full, 128);
+    for (int i = 0; i < 4; ++i) mbar_init(&ctl.res_full[i], kGatherThreads);
+    mbar_init(&ctl.res2_full, kGatherThreads);
     for (int s2 = 0; s2 < 2; ++s2) {
-      mbar_init(&ctl.kst_full[s2], 128);
+      mbar_init(&ctl.kst_full[s2], kGatherThreads);
       mbar_init(&ctl.kst_empty[s2], 1);
       mbar_init(&ctl.q_full[s2], 1);
       mbar_init(&ctl.q_empty[s2], 1);
@@ -538,31 +547,36 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     bool ok = true;
 
-    // gatherers (warps 4..7): thread gt copies 16-byte chunk gc of rows
-    // gr0 + 16 k of every slab
-    const int gt = tid - 128;
-    const int gr0 = (gt >> 3) & 15, gc = gt & 7;
+    // gatherers (the last kGatherWarps warps; warps 0 and 1 carry the MMA
+    // and Q-load threads): thread gt copies 16-byte chunk gc of rows
+    // gr0 + kGatherThreads / 8 k of every slab
+    const bool gatherer = warp >= kThreads / 32 - kGatherWarps;
+    const int gt = tid - (kThreads - kGatherThreads);
+    const int gstep = kGatherThreads / 8;
+    const int gr0 = gt >> 3, gc = gt & 7;
     const int fr0 = gt >> 2, fc4 = gt & 3;  // fp8 cache: rows fr0 + 32 k, 16-byte chunk fc4
-    const int iters = npad >> 4;
     float ks0 = 0.f, ks1 = 0.f;
-    if (warp >= 4) {
+    if (gatherer) {
       const int32_t* crow = p.cidx + (int64_t)q * p.topk + slice * kItemKeys;
-      const int32_t i0 = gt < n ? __ldcg(crow + gt) : 0;
-      const int32_t i1 = gt + 128 < n ? __ldcg(crow + gt + 128) : 0;
-      ctl.kidx[gt] = i0;
-      ctl.kidx[gt + 128] = i1;
-      if (FP8) {  // stored once S is complete (they go where Q was staged)
+      if (FP8) {
+        const int32_t i0 = gt < n ? __ldcg(crow + gt) : 0;
+        const int32_t i1 = gt + 128 < n ? __ldcg(crow + gt + 128) : 0;
+        ctl.kidx[gt] = i0;
+        ctl.kidx[gt + 128] = i1;
+        // stored once S is complete (they go where Q was staged)
         ks0 = gt < n ? __ldg(p.kv_scale + i0) : 0.f;
         ks1 = gt + 128 < n ? __ldg(p.kv_scale + i1) : 0.f;
+      } else {
+        for (int r = gt; r < kItemKeys; r += kGatherThreads) ctl.kidx[r] = r < n ? __ldcg(crow + r) : 0;
       }
-      bar_gather();
+      bar_gather<kGatherThreads>();
     }
 
-    if (warp >= 4) {
+    if (gatherer) {
       auto gather = [&](int slot, int slab) {
         if (ok) {
           if (FP8) stage_slab_fp8(slot_u32(slot), kv8, ctl.kidx, npad, n, fr0, fc4, slab);
-          else gather_slab(slot_u32(slot), kv, ctl.kidx, iters, n, gr0, gc, slab);
+          else gather_slab(slot_u32(slot), kv, ctl.kidx, npad, gstep, n, gr0, gc, slab);
         }
         cp_async_commit();
       };
@@ -580,7 +594,7 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       gather(3, 3);  // G5
       // the ring refills (slabs 5, 6, 7) wait for free slots: start their
       // DRAM reads now so that the copies find them in L2
-      for (int r = gt; r < n; r += 128) {
+      for (int r = gt; r < n; r += kGatherThreads) {
         const int64_t row = (int64_t)ctl.kidx[r] * kDqk;
         if (FP8) {  // bytes [320, 512): every 128-byte line holds one of these
           prefetch_l2(kv8 + row + 5 * kSlab);
@@ -682,7 +696,7 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     float* s_ks = reinterpret_cast<float*>(s_qst + kScaleOffset);
     float* s_kc = s_ks + kItemKeys;
     if (FP8) {
-      if (warp >= 4) {
+      if (gatherer) {
         // keys past n: scale 0 (P = 0) and logit factor 1 (their -inf mask
         // must not meet a zero factor)
         s_ks[gt] = ks0;
@@ -887,15 +901,15 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     ok = mbar_wait(&ctl.oa_full, 0, p.err, kErrWaitMma) && ok;
     __syncwarp();
     tc_fence_after();
-    if (warp >= 4) {
+    if (gatherer) {
       // slabs 4, 5 over R2, R3 (A has read them), landing while A is stored
       if (ok) {
         if (FP8) {
           stage_slab_fp8(slot_u32(2), kv8, ctl.kidx, npad, n, fr0, fc4, 4);
           stage_slab_fp8(slot_u32(3), kv8, ctl.kidx, npad, n, fr0, fc4, 5);
         } else {
-          gather_slab(slot_u32(2), kv, ctl.kidx, iters, n, gr0, gc, 4);
-          gather_slab(slot_u32(3), kv, ctl.kidx, iters, n, gr0, gc, 5);
+          gather_slab(slot_u32(2), kv, ctl.kidx, npad, gstep, n, gr0, gc, 4);
+          gather_slab(slot_u32(3), kv, ctl.kidx, npad, gstep, n, gr0, gc, 5);
         }
       }
       cp_async_commit();
