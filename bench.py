@@ -25,6 +25,7 @@ region.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -998,10 +999,16 @@ class Bench:
         sleep = getattr(torch.cuda, "_sleep", None)
         if sleep is not None:  # about 30 us of host time per queued call
             sleep(int(2.0e9 * (0.002 + min(steps, 2000) * 30e-6)))
-        e0.record()
-        for i in range(steps):
-            self.r.call(i, mode)
-        e1.record()
+        gc_was = gc.isenabled()
+        gc.disable()  # a collection pause longer than the sleep would idle the device
+        try:
+            e0.record()
+            for i in range(steps):
+                self.r.call(i, mode)
+            e1.record()
+        finally:
+            if gc_was:
+                gc.enable()
         self.barrier()
         return max_over_ranks(e0.elapsed_time(e1), self.dist, "cuda")
 
@@ -1016,24 +1023,34 @@ class Bench:
         sleep = getattr(torch.cuda, "_sleep", None)
         if sleep is not None:  # about 60 us of host time per queued call
             sleep(int(2.0e9 * (0.005 + steps * 60e-6)))
-        for i in range(steps):
-            starts[i].record()
-            self.r.call(i, mode)
-            ends[i].record()
+        gc_was = gc.isenabled()
+        gc.disable()
+        try:
+            for i in range(steps):
+                starts[i].record()
+                self.r.call(i, mode)
+                ends[i].record()
+        finally:
+            if gc_was:
+                gc.enable()
         self.barrier()
         return [s_.elapsed_time(e_) * 1000.0 for s_, e_ in zip(starts, ends)]
 
     def sink_cost(self, steps):
         """Timed regions of back-to-back calls in the workload's mode and with
         sinks disabled, in alternating rounds so that a drift in clocks or in
-        the machine's other load falls on both alike; and the medians of
-        isolated launches of both modes, alternating in the same way."""
+        the machine's other load falls on both alike (the ratio of the two
+        modes' median rounds); and the medians of isolated launches of both
+        modes, alternating in the same way."""
         rounds = 4
         per_round = max(steps // rounds, 10)
-        t_mode = t_none = 0.0
+        t_modes, t_nones = [], []
         for _ in range(rounds):
-            t_mode += self.timed(self.r.mode, per_round)
-            t_none += self.timed(W.SINK_NONE, per_round)
+            t_modes.append(self.timed(self.r.mode, per_round))
+            t_nones.append(self.timed(W.SINK_NONE, per_round))
+        # medians over the rounds: one round disturbed by the host (a pause
+        # longer than the device sleep ahead of it) does not count
+        t_mode, t_none = statistics.median(t_modes), statistics.median(t_nones)
         ndev = max(min(steps, 500), 10)
         chunk = min(ndev, 50)
         per, per_none = [], []
