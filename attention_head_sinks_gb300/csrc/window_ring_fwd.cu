@@ -16,7 +16,10 @@
 // producer loads only those new blocks into a ring of NR slots, so K and V are
 // read from memory about once.
 //
-// Warps: 0 = TMA producer, 1 = MMA issuer, 2 = TMEM owner, 4..7 and 8..11 =
+// Warps: 0 = TMA producer of Q and of the even ring blocks, 1 = MMA issuer,
+// 2 = TMEM owner, 3 = TMA producer of the odd ring blocks (one thread's TMA
+// copies complete one after another, about one transaction per 0.3 us, so
+// the ring refills go through two issuing threads), 4..7 and 8..11 =
 // softmax warpgroups 0 and 1, which take alternate items.  Tensor memory: two
 // 256-column buffers (one per warpgroup), each holding S [128 x NBT*KB] at
 // column 0, P (bf16) in place over it, and O [128 x D] at column 128.
@@ -240,8 +243,12 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_qc,
   const uint32_t tmem = ctl.tmem_base;
   griddep_wait();  // set-up above overlaps the previous kernel; memory from here
 
-  if (tid == 0) {
-    // ---- TMA producer ------------------------------------------------------
+  if (tid == 0 || tid == 96) {
+    // ---- TMA producers: thread 0 loads Q and the even ring blocks, thread
+    // 96 the odd ones (each thread's copies complete one after another);
+    // both walk every item and keep the same sequence numbers
+    const int par = tid == 0 ? 0 : 1;
+    const bool do_q = tid == 0;
     tma_prefetch_map(&tm_qc);
     if (S::NT) tma_prefetch_map(&tm_qt);
     tma_prefetch_map(&tm_kc);
@@ -253,20 +260,23 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_qc,
     for (int it = 0; it < n && ok; ++it) {
       const ItemInfo info = walk_item<S::NEWB>(w, cta_item_u(ci, it, p), p);
       const int qs = it % kNQ;
-      if (it >= kNQ) ok = mbar_wait(&ctl.q_empty[qs], ((it / kNQ) - 1) & 1, p.err, kErrWaitFree);
-      if (!ok) break;
-      mbar_arrive_expect_tx(&ctl.q_full[qs], S::QBYTES);
-      uint8_t* qst = sQ + qs * S::QBYTES;
+      if (do_q) {
+        if (it >= kNQ) ok = mbar_wait(&ctl.q_empty[qs], ((it / kNQ) - 1) & 1, p.err, kErrWaitFree);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&ctl.q_full[qs], S::QBYTES);
+        uint8_t* qst = sQ + qs * S::QBYTES;
 #pragma unroll
-      for (int c = 0; c < S::NC; ++c)
-        tma_load_3d(qst + c * S::QC, &tm_qc, &ctl.q_full[qs], 64 * c, info.g * G, info.j * S::TQ);
+        for (int c = 0; c < S::NC; ++c)
+          tma_load_3d(qst + c * S::QC, &tm_qc, &ctl.q_full[qs], 64 * c, info.g * G, info.j * S::TQ);
 #pragma unroll
-      for (int t = 0; t < S::NT; ++t)
-        tma_load_3d(qst + S::NC * S::QC + t * S::QT, &tm_qt, &ctl.q_full[qs], 64 * S::NC + 16 * t,
-                    info.g * G, info.j * S::TQ);
-      ++nq;
+        for (int t = 0; t < S::NT; ++t)
+          tma_load_3d(qst + S::NC * S::QC + t * S::QT, &tm_qt, &ctl.q_full[qs], 64 * S::NC + 16 * t,
+                      info.g * G, info.j * S::TQ);
+        ++nq;
+      }
       const int bl = info.bf + p.nbt - 1;
       for (int b = info.same_run ? last_bl + 1 : info.bf; b <= bl; ++b, ++seq) {
+        if ((seq & 1) != par) continue;
         const int slot = seq % NR;
         if (seq >= NR) ok = mbar_wait(&ctl.kv_empty[slot], ((seq / NR) - 1) & 1, p.err, kErrWaitFree);
         if (!ok) break;
@@ -289,7 +299,7 @@ window_ring_kernel(const __grid_constant__ CUtensorMap tm_qc,
     // Bounded drain: every copy issued must have landed before the CTA exits
     // (immediate when the MMA warp consumed them all).
     for (int sq = max(0, seq - NR); sq < seq; ++sq)
-      mbar_wait(&ctl.kv_full[sq % NR], (sq / NR) & 1, p.err, kErrWaitDrain);
+      if ((sq & 1) == par) mbar_wait(&ctl.kv_full[sq % NR], (sq / NR) & 1, p.err, kErrWaitDrain);
     for (int it = max(0, nq - kNQ); it < nq; ++it)
       mbar_wait(&ctl.q_full[it % kNQ], (it / kNQ) & 1, p.err, kErrWaitDrain);
   } else if (tid == 32 && n > 0) {
