@@ -67,7 +67,7 @@ def test_noalloc_matches_oracle_on_two_calls():
 
 def test_noalloc_after_a_larger_layout():
     """A call that fills the array with a large layout (top-4096 lists, so
-    queries with more than eight 256-key items take the warp-unit combine),
+    queries with more than eight 256-key items take the plain-load merge),
     then one with fewer heads (another head stride), fewer queries and
     another list length, which finds the first call's contents in place."""
     import attention_head_sinks_gb300 as sa
