@@ -75,7 +75,7 @@ constexpr int kMergeStages = 3; // merge units in flight per CTA (TMA-fed)
 constexpr int kPartChunk = 32;  // V columns sharing one fp16 scale in a partial
 
 // One merge unit's partials in shared memory (row stride: the tile's head
-// count): the [8 items][8 column pairs][128 heads] O box (fp16 pairs) and the
+// count): the [8 items][16 column pairs][128 heads] O box (fp16 pairs) and the
 // [8 items][128 heads] scale exponents of the unit's 32-column chunk.
 struct __align__(128) MergeStage {
   uint32_t o[kMergeGroup][kMergeCols / 2][128];
@@ -968,11 +968,11 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   }  // items
 
   // ---- split-KV merge -------------------------------------------------------------
-  // Units of (query with several items, block of 128 heads, 16 V columns),
-  // 256 queries at a time, split into one contiguous range per CTA with
-  // about equal partial bytes per CTA (a unit weighs the items it loads), so
-  // a CTA's units mostly share a query: it waits for one counter and loads
-  // one (m, l) box per run, not one per unit.  A unit waits (bounded) until
+  // Units of (query with several items, block of 128 heads, 32 V columns:
+  // one scale chunk), 256 queries at a time, split into one contiguous range
+  // of about equal unit count per CTA, so a CTA's units mostly share a query:
+  // it waits for one counter and loads one (m, l) box per run, not one per
+  // unit.  A unit waits (bounded) until
   // every item of its query is counted.  Thread t merges head t mod 128 of
   // the unit's head block, half t / 128 of the unit's V columns:
   //   O = sum_s 2^(m_s - M) O_s * alpha / (L alpha + 2^(s_h log2e - M')),
