@@ -137,6 +137,11 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 __device__ __forceinline__ void bar_softmax() {  // the eight softmax warps
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
+// The two softmax warps that share a TMEM lane quadrant (warps w and w + 4,
+// the two blocks of a step for the same 32 rows): named barrier 2 + w mod 4.
+__device__ __forceinline__ void bar_softmax_pair(int warp) {
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + (warp & 3)) : "memory");
+}
 
 __device__ __forceinline__ int upper_doc(const int32_t* cu, int n, int t) {
   int lo = 0, hi = n - 1;  // largest e with cu[e] <= t
@@ -578,7 +583,8 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
           mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * c2;
         }
         ctl.red_m[st][part][row] = mx;
-        bar_softmax();
+        // only the two warps of these rows meet: the row max of the step
+        bar_softmax_pair(warp);
         mx = fmaxf(ctl.red_m[st][0][row], ctl.red_m[st][1][row]);
         // lazy rescale of O and l when this row's max grew by more than 2^8
         const bool need = mx > m_use + kRescaleThreshold;
