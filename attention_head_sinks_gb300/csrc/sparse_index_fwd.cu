@@ -757,7 +757,8 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       red.m[part][row] = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
     }
-    __syncthreads();
+    // only the two warps of the same rows (w and w + 4) exchange the max
+    asm volatile("bar.sync %0, 64;" ::"r"(2 + (warp & 3)) : "memory");
     // max(s) * c2 == max(s * c2) exactly (c2 > 0, rounding is monotone); the
     // fp8 maxima are already in the log2 domain
     const float m = fmaxf(red.m[0][row], red.m[1][row]) * (FP8 ? 1.f : c2);
