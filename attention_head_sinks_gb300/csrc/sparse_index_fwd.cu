@@ -159,6 +159,7 @@ struct __align__(8) IndexSmemCtl {
   int32_t merge_ok;
   int32_t merge_range[2];    // this CTA's merge units [first, end) of a chunk
   uint64_t merge_full[kMergeStages];
+  uint64_t merge_free[kMergeStages];  // every warp has read the stage
   int32_t scan_f[8], scan_p[8];
   int32_t kidx[kItemKeys];  // the item's key rows
 };
@@ -1002,7 +1003,10 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     // (the softmax exchange); order those writes before the copies' writes
     fence_proxy_async();
     if (tid == 0) {
-      for (int i = 0; i < kMergeStages; ++i) mbar_init(&ctl.merge_full[i], 1);
+      for (int i = 0; i < kMergeStages; ++i) {
+        mbar_init(&ctl.merge_full[i], 1);
+        mbar_init(&ctl.merge_free[i], kThreads / 32);
+      }
       fence_mbar_init();
       tma_prefetch_map(&tm_part);
       tma_prefetch_map(&tm_part1);
@@ -1130,7 +1134,8 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int st = (int)(k % kMergeStages);
             int q, ns, hb, cb;
             unit_of(k, q, ns, hb, cb);
-            if (!mbar_wait(&ctl.merge_full[st], (phase >> st) & 1u, p.err, kErrWaitLoad))
+            const uint32_t use_par = (phase >> st) & 1u;  // this use of stage st
+            if (!mbar_wait(&ctl.merge_full[st], use_par, p.err, kErrWaitLoad))
               ctl.merge_ok = 0;
             phase ^= 1u << st;
             const int con_ml = (int)(((first + k) / kUnitsPerHb - first / kUnitsPerHb) & 1);
@@ -1170,8 +1175,15 @@ sparse_index_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
               for (int g = 0; g < kMergeSegs; ++g)
                 finish(q, h, cb * kMergeCols + (half * kMergeSegs + g) * 8, M, L, acc[g]);
             }
-            __syncthreads();  // stage st is consumed
-            if (lane0_of_stage == st && k + kMergeStages < mine) issue(k + kMergeStages, st);
+            // stage st is consumed by this warp; its filler waits for every warp
+            // (the warps need not wait for each other)
+            __syncwarp();
+            if ((tid & 31) == 0) mbar_arrive(&ctl.merge_free[st]);
+            if (lane0_of_stage == st && k + kMergeStages < mine) {
+              if (!mbar_wait(&ctl.merge_free[st], use_par, p.err, kErrWaitFree))
+                ctl.merge_ok = 0;
+              issue(k + kMergeStages, st);
+            }
           }
         } else {
           for (int64_t k = 0; k < mine; ++k) {
