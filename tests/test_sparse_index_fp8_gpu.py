@@ -9,7 +9,8 @@ Covers the full 64-query x 128-head decode workload over an fp8 cache with
 the -inf no-op, bitwise agreement with the bf16 path on power-of-two scales
 (the dequantised rows are then bf16 values and the scale commutes with every
 rounding), ragged and repeated lists, head counts off one 128-row block,
-more than eight 256-key items per query, and caches that hold every non-NaN
+more than eight 256-key items per query, the longest accepted list (topk
+8192), and caches that hold every non-NaN
 e4m3 code (subnormals, both zeros, +-448) under row scales over 16 octaves.
 """
 import numpy as np
@@ -143,6 +144,13 @@ def test_all_lists_full():
 def test_more_than_eight_items():
     c = W.index_fp8_case(4, 40, 576, 512, 9000, 3000, (2900, 300, 2100, 7), (-2.2, 2.49),
                          NULL, 3900, "many_items_fp8")
+    check(c, NULL)
+
+
+def test_maximum_topk():
+    # topk 8192, the longest accepted list: 32 items for the full list
+    c = W.index_fp8_case(3, 128, 576, 512, 20000, 8192, (8192, 5, 8000), (-2.2, 2.49),
+                         NULL, 3901, "max_topk_fp8")
     check(c, NULL)
 
 

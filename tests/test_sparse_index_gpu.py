@@ -5,7 +5,8 @@ valid keys per query (afierka-intel/vllm pull 76, Why / Test plan), the
 -inf no-op, empty rows, -1 padding anywhere in the row, out-of-range and
 repeated indices, lists that end inside a slice, head counts below and above
 one 128-row block, more than 256 queries, more than eight 256-key items per
-query, and workspace reuse across calls.
+query, the longest accepted list (topk 8192, 32 items), and workspace reuse across
+calls.
 """
 import numpy as np
 import pytest
@@ -207,4 +208,14 @@ def test_more_than_eight_items(hq):
     # (the merge path for more than eight items), 300 gives 2, 7 gives 1
     c = W.index_case(4, hq, 576, 512, 9000, 3000, (2900, 300, 2100, 7), (-2.2, 2.49),
                      NULL, 3500 + hq, "many_items")
+    check(c, NULL)
+
+
+@pytest.mark.parametrize("hq", [128, 40])
+def test_maximum_topk(hq):
+    # the longest list the entry point accepts (topk 8192): a full list is 32
+    # items of 256 keys, merged eight items at a time; 8191 valid keys end one
+    # key short of the last item; a single key needs no merge
+    c = W.index_case(3, hq, 576, 512, 20000, 8192, (8192, 1, 8191), (-2.2, 2.49), NULL,
+                     3700 + hq, "max_topk")
     check(c, NULL)
