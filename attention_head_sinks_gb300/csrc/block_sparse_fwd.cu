@@ -647,10 +647,15 @@ block_sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (lane == 0) mbar_arrive(&ctl.p_full[st]);
       }
       if (nsteps > 0) {
-        // O is final once the last P V is done; S(last), whose completion is
+        // O is final once the last P V is done.  S(last), whose completion is
         // all this thread has seen, went to the pipe before the P V of the
-        // last kSBufs - 1 steps, so wait for each of those
-        for (int k = max(0, nsteps - kSBufs); k < nsteps; ++k) ok = wait_pv(gs + k) && ok;
+        // last kSBufs steps.  P V(last - 2) is not waited for by itself: its
+        // barrier also carries P V(last), and a parity wait for it that began
+        // after P V(last) had completed would wait for a phase that never
+        // comes.  One thread issues every P V and each commit arrives only
+        // after that thread's earlier MMAs, so once P V(last - 1) is seen,
+        // P V(last - 2) has arrived and the wait for P V(last) is exact.
+        for (int k = max(0, nsteps - 2); k < nsteps; ++k) ok = wait_pv(gs + k) && ok;
         __syncwarp();
         tc_fence_after();
       }
